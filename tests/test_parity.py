@@ -1,0 +1,260 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (per matrix, relative Frobenius error against the oracle's fp64
+result on the same input values): 2e-2 for the bf16 tensor-core path, 1e-5 for
+the fp32 validation path. Indexing and reassembly are checked bit-exactly with
+maps whose result is exactly representable (identity coefficients, K = 0 with
+no normalisation), and tile independence by perturbing one tile.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_newton_schulz_03_b300 as hm
+from tiled_newton_schulz_03_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_FP32 = 1e-5
+
+
+def rel_fro(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    return float(np.linalg.norm(got - want) / np.linalg.norm(want))
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from tiled_newton_schulz_03_b300 import build
+    build.build()
+    hm.load_library()
+    yield
+    torch.cuda.synchronize()
+    assert hm.device_error() == 0
+
+
+# ---------------------------------------------------------------- one matrix
+
+@pytest.mark.parametrize("T,path,tol", [(128, "tensor", TOL_BF16), (64, "fp32", TOL_FP32),
+                                        (128, "fp32", TOL_FP32), (32, "fp32", TOL_FP32)])
+def test_gaussian_fp32_256x512(T, path, tol):
+    G = synth.gaussian(256, 512, seed=0)            # fp32, N(0, 1)
+    out = hm.tiled_ns(G.cuda(), T, 5, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
+    assert rel_fro(f64(out), want) <= tol
+
+
+@pytest.mark.parametrize("H,W", [(300, 530), (128, 128), (1, 1), (1, 300), (257, 3),
+                                 (129, 255), (768, 3072)])
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_lowrank_bf16_ragged(H, W, path):
+    G = synth.lowrank_noise(H, W, seed=H * 7 + W)
+    out = hm.tiled_ns(G.cuda(), 128, 5, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), 128, 5)
+    assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
+
+
+@pytest.mark.parametrize("K", [0, 1, 3])
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_small_K(K, path):
+    G = synth.lowrank_noise(200, 300, seed=K + 40)
+    out = hm.tiled_ns(G.cuda(), 128, K, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), 128, K)
+    tol = TOL_BF16 if (path == "tensor" and K > 0) else TOL_FP32
+    assert rel_fro(f64(out), want) <= tol
+
+
+@pytest.mark.parametrize("norm", ["matrix", "none"])
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_norm_modes(norm, path):
+    G = synth.lowrank_noise(256, 384, seed=5)
+    if norm == "none":
+        G = (G.float() / G.float().norm() * 0.5).to(torch.bfloat16)   # keep the map stable
+    out = hm.tiled_ns(G.cuda(), 128, 5, norm=norm, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), 128, 5, norm=norm)
+    assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
+
+
+def test_other_coefficients():
+    G = synth.lowrank_noise(256, 256, seed=8)
+    coeffs = (1.5, -0.5, 0.0)
+    out = hm.tiled_ns(G.cuda(), 128, 8, coeffs=coeffs, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), 128, 8, coeffs)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+
+
+# ---------------------------------------------------------------- bit-exact structure
+
+@pytest.mark.parametrize("H,W", [(300, 530), (129, 1), (1000, 3000)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_identity_map_is_bit_exact(H, W, dtype):
+    G = synth.gaussian(H, W, seed=3, dtype=dtype).cuda()
+    for K, coeffs in ((0, hm.QUINTIC), (3, (1.0, 0.0, 0.0))):
+        out = hm.tiled_ns(G, 128, K, coeffs=coeffs, norm="none", out_dtype=dtype)
+        assert torch.equal(out, G)
+
+
+def test_fp32_in_bf16_out_rounds_once():
+    G = synth.gaussian(130, 260, seed=4).cuda()
+    out = hm.tiled_ns(G, 128, 0, norm="none", out_dtype=torch.bfloat16)
+    assert torch.equal(out, G.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_perturbing_one_tile_leaves_others_bit_identical(path):
+    G = synth.lowrank_noise(384, 512, seed=9).cuda()
+    base = hm.tiled_ns(G, 128, 5, path=path)
+    G2 = G.clone()
+    G2[130:140, 260:300] += 0.01          # tile (1, 2)
+    pert = hm.tiled_ns(G2, 128, 5, path=path)
+    mask = torch.ones_like(G, dtype=torch.bool)
+    mask[128:256, 256:384] = False
+    assert torch.equal(base[mask], pert[mask])
+    assert not torch.equal(base[~mask], pert[~mask])
+
+
+def test_in_place_equals_out_of_place():
+    G = synth.lowrank_noise(300, 400, seed=10).cuda()
+    ref = hm.tiled_ns(G, 128, 5)
+    X = G.clone()
+    hm.tiled_ns(X, 128, 5, out=X)
+    assert torch.equal(X, ref)
+
+
+def test_unaligned_leading_dimension():
+    # ld = 50257 bf16 elements: rows are not 16-byte aligned (scalar-load path).
+    base = synth.lowrank_noise(256, 50257, seed=11).cuda()
+    view = base[:, 1000:1300]               # 256 x 300, ld 50257, odd offset
+    out = hm.tiled_ns(view, 128, 5, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(view), 128, 5)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+    ref = hm.tiled_ns(view.contiguous(), 128, 5, out_dtype=torch.float32)
+    assert torch.equal(out, ref)
+
+
+# ---------------------------------------------------------------- batching, chunking
+
+def test_batched_equals_single_calls_and_oracle():
+    shapes = [(768, 768), (3072, 768), (768, 3072), (200, 130), (1, 5)]
+    Gs = [synth.lowrank_noise(H, W, seed=20 + i).cuda() for i, (H, W) in enumerate(shapes)]
+    outs = hm.tiled_ns_batched(Gs, 128, 5, out_dtype=torch.float32)
+    for G, O in zip(Gs, outs):
+        single = hm.tiled_ns(G, 128, 5, out_dtype=torch.float32)
+        assert torch.equal(O, single)
+        assert rel_fro(f64(O), oracle.tiled_ns(f64(G), 128, 5)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_chunking_does_not_change_result(path):
+    shapes = [(512, 512), (256, 768), (384, 130)]
+    Gs = [synth.lowrank_noise(H, W, seed=30 + i).cuda() for i, (H, W) in enumerate(shapes)]
+    ref = hm.tiled_ns_batched(Gs, 128, 5, path=path)
+    for chunk in (1, 128 * 128 * 2, 5 * 128 * 128 * 2 + 7, 10 ** 9):
+        outs = hm.tiled_ns_batched(Gs, 128, 5, path=path, chunk_bytes=chunk)
+        for a, b in zip(ref, outs):
+            assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- fused step
+
+def _step_case(shapes, seed, mdtype=torch.float32, wdtype=torch.bfloat16):
+    Ws = [synth.gaussian(H, W, seed + i, std=0.02, dtype=wdtype).cuda() for i, (H, W) in enumerate(shapes)]
+    Gs = [synth.lowrank_noise(H, W, seed=seed + 100 + i).cuda() for i, (H, W) in enumerate(shapes)]
+    Ms = [synth.gaussian(H, W, seed + 200 + i, std=1e-3, dtype=mdtype).cuda() for i, (H, W) in enumerate(shapes)]
+    return Ws, Gs, Ms
+
+
+@pytest.mark.parametrize("path", ["tensor", "fp32"])
+def test_step_matches_oracle(path):
+    shapes = [(768, 768), (3072, 768), (300, 530)]
+    Ws, Gs, Ms = _step_case(shapes, 50)
+    W0 = [f64(w) for w in Ws]
+    M0 = [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, 128, 5, lr=0.02, mu=0.95, nesterov=True, path=path)
+    for i, (H, W) in enumerate(shapes):
+        Wn, Mn, O = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 128, 5, lr=0.02, mu=0.95)
+        # momentum: one fp32 FMA per element
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        # update direction, with the bf16 rounding of W_new added to the bound
+        d_gpu = f64(Ws[i]) - W0[i]
+        d_ref = Wn - W0[i]
+        tol = TOL_BF16 if path == "tensor" else TOL_FP32
+        bound = tol * np.linalg.norm(d_ref) + np.linalg.norm(np.abs(Wn) * 2.0 ** -8)
+        assert np.linalg.norm(d_gpu - d_ref) <= bound
+        assert rel_fro(f64(Ws[i]), Wn) <= tol
+
+
+def test_step_zero_lr_keeps_weights_and_updates_momentum():
+    Ws, Gs, Ms = _step_case([(256, 384)], 60)
+    W0 = Ws[0].clone()
+    M0 = f64(Ms[0])
+    hm.step(Ws, Gs, Ms, 128, 5, lr=0.0, mu=0.9)
+    assert torch.equal(Ws[0], W0)
+    assert rel_fro(f64(Ms[0]), 0.9 * M0 + f64(Gs[0])) <= 1e-6
+
+
+def test_step_three_successive_steps_with_tile_schedule():
+    shapes = [(1000, 3000 // 4), (2048, 503)]
+    Ws, _, Ms = _step_case(shapes, 70)
+    Wr = [f64(w) for w in Ws]
+    Mr = [f64(m) for m in Ms]
+    sched = hm.TSchedule([(0, 128), (1, 128), (2, 128)])
+    for s in range(3):
+        Gs = [synth.lowrank_noise(H, W, seed=1000 * s + i).cuda() for i, (H, W) in enumerate(shapes)]
+        T = sched(s)
+        hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95)
+        for i in range(len(shapes)):
+            Wr[i], Mr[i], _ = oracle.himuon_step(Wr[i], f64(Gs[i]), Mr[i], T, 5, lr=0.02, mu=0.95)
+    for i in range(len(shapes)):
+        assert rel_fro(f64(Ws[i]), Wr[i]) <= TOL_BF16
+        assert rel_fro(f64(Ms[i]), Mr[i]) <= 1e-5
+
+
+def test_step_weight_decay_and_fp32_weights():
+    Ws, Gs, Ms = _step_case([(256, 256)], 80, wdtype=torch.float32)
+    W0, M0 = f64(Ws[0]), f64(Ms[0])
+    hm.step(Ws, Gs, Ms, 128, 5, lr=0.01, mu=0.9, weight_decay=0.1, nesterov=False,
+            scale_mode="none")
+    Wn, _, _ = oracle.himuon_step(W0, f64(Gs[0]), M0, 128, 5, lr=0.01, mu=0.9, nesterov=False,
+                                  weight_decay=0.1, scale_mode="none")
+    d_gpu, d_ref = f64(Ws[0]) - W0, Wn - W0
+    assert np.linalg.norm(d_gpu - d_ref) <= TOL_BF16 * np.linalg.norm(d_ref)
+
+
+# ---------------------------------------------------------------- errors
+
+def test_bad_arguments_raise_without_launch():
+    G = torch.zeros(4, 4, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(hm.HimuonError) as e:
+        hm.tiled_ns(G, 0, 5)
+    assert e.value.status_name == "INVALID_ARG"
+    with pytest.raises(hm.HimuonError):
+        hm.tiled_ns(G, 128, 65)
+    with pytest.raises(hm.HimuonError):
+        hm.tiled_ns(G, 128, 5, out=G[:, :3])
+    with pytest.raises(hm.HimuonError) as e:
+        hm.tiled_ns(G, 96, 5)                        # no tensor kernel for T = 96
+    assert e.value.status_name == "UNSUPPORTED"
+    big = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(hm.HimuonError):               # partial overlap of out and G
+        hm.tiled_ns(big[:, :4], 128, 5, out=big[:, 2:6])
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    h = hm.Handle()
+    hm.set_wait_limit(1_000_000, handle=h)           # 1 ms
+    hm.wait_selftest(handle=h)
+    assert hm.device_error(handle=h) == 4            # HIMUON_ERR_TIMEOUT
+    assert hm.device_error(handle=h) == 0            # cleared
+    G = synth.lowrank_noise(128, 128, seed=1).cuda()
+    out = hm.tiled_ns(G, 128, 5, handle=h, out_dtype=torch.float32)
+    assert rel_fro(f64(out), oracle.tiled_ns(f64(G), 128, 5)) <= TOL_BF16
+    h.close()

@@ -1,0 +1,489 @@
+// C ABI of libhimuon (declared in include/himuon.h): argument checks, the
+// cross-layer work plan (flat tile list over all matrices), memory-bounded
+// chunking, workspace management and kernel dispatch.
+//
+// Method: "Hierarchical Muon: Tiled Newton-Schulz Updates for Efficient Muon
+// Optimization", abstract: tiles are independent (sentences 3-4), so the tiles
+// of any number of matrices form one work list (cross-layer batching) that can
+// be cut anywhere into launches (memory-bounded chunking), and T may differ from
+// call to call (runtime tile-size schedules) -- sentence 6.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/himuon.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace himuon;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+himuon_status fail(himuon_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+himuon_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(HIMUON_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+constexpr int32_t kMaxK = 64;
+constexpr int64_t kMaxDim = (1LL << 31) - 1024;
+constexpr size_t kFp32ScratchCap = size_t(512) << 20;  // bytes of fp32-path scratch per sub-batch
+
+bool valid_dtype(int32_t t) { return t == HIMUON_BF16 || t == HIMUON_FP32; }
+int64_t esize(int32_t t) { return t == HIMUON_FP32 ? 4 : 2; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p, int64_t ld, int32_t t) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * esize(t)) % 16 == 0);
+}
+
+// Byte range [lo, hi) touched by an H x W matrix with leading dimension ld.
+void byte_range(const void* p, int64_t H, int64_t W, int64_t ld, int32_t t, uintptr_t* lo,
+                uintptr_t* hi) {
+  *lo = reinterpret_cast<uintptr_t>(p);
+  *hi = *lo + static_cast<uintptr_t>(((H - 1) * ld + W) * esize(t));
+}
+
+bool overlaps(const void* a, int64_t H, int64_t W, int64_t lda, int32_t ta, const void* b,
+              int64_t ldb, int32_t tb) {
+  uintptr_t a0, a1, b0, b1;
+  byte_range(a, H, W, lda, ta, &a0, &a1);
+  byte_range(b, H, W, ldb, tb, &b0, &b1);
+  return a0 < b1 && b0 < a1;
+}
+
+himuon_status check_ns_params(const himuon_ns_params& p) {
+  if (!(p.norm == HIMUON_NORM_TILE || p.norm == HIMUON_NORM_MATRIX || p.norm == HIMUON_NORM_NONE))
+    return fail(HIMUON_ERR_INVALID_ARG, "ns params: unknown norm mode");
+  if (!(p.path == HIMUON_PATH_AUTO || p.path == HIMUON_PATH_TENSOR || p.path == HIMUON_PATH_FP32))
+    return fail(HIMUON_ERR_INVALID_ARG, "ns params: unknown path");
+  if (!std::isfinite(p.a) || !std::isfinite(p.b) || !std::isfinite(p.c))
+    return fail(HIMUON_ERR_INVALID_ARG, "ns params: coefficients must be finite");
+  if (!(p.eps >= 0.f) || !std::isfinite(p.eps))
+    return fail(HIMUON_ERR_INVALID_ARG, "ns params: eps must be finite and >= 0");
+  return HIMUON_OK;
+}
+
+himuon_status check_shape(int64_t H, int64_t W, int64_t ld, const char* what) {
+  if (H < 1 || W < 1) return fail(HIMUON_ERR_INVALID_ARG, std::string(what) + ": H and W must be >= 1");
+  if (H > kMaxDim || W > kMaxDim) return fail(HIMUON_ERR_INVALID_ARG, std::string(what) + ": H or W too large");
+  if (ld < W) return fail(HIMUON_ERR_INVALID_ARG, std::string(what) + ": leading dimension < W");
+  return HIMUON_OK;
+}
+
+}  // namespace
+
+struct himuon_handle {
+  int device = -1;
+  int num_sms = 0;
+  void* ws = nullptr;          // descriptor table, part offsets, norm partials
+  size_t ws_bytes = 0;
+  float* scratch = nullptr;    // fp32-path tile buffers
+  size_t scratch_bytes = 0;
+  int* d_err = nullptr;        // device error word
+  uint64_t wait_ns = 2000000000ull;
+  int64_t launches = 0;        // kernels launched through this handle
+  std::vector<unsigned char> host;
+};
+
+namespace {
+
+himuon_status grow(void** buf, size_t* have, size_t need, cudaStream_t stream, const char* what) {
+  if (need <= *have) return HIMUON_OK;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace growth: stream sync");
+  const size_t n = std::max(need, *have + *have / 2);
+  if (*buf) cudaFree(*buf);
+  *buf = nullptr;
+  *have = 0;
+  e = cudaMalloc(buf, n);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *buf = nullptr;
+    return fail(HIMUON_ERR_OUT_OF_MEMORY, std::string(what) + ": cudaMalloc failed");
+  }
+  *have = n;
+  return HIMUON_OK;
+}
+
+himuon_status check_handle(himuon_handle* h) {
+  if (!h) return fail(HIMUON_ERR_INVALID_ARG, "handle is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(HIMUON_ERR_INVALID_ARG, "handle was created on another device than the current one");
+  return HIMUON_OK;
+}
+
+// Runs the tiled NS map (or the fused step) over the matrices in `descs`.
+himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T, int32_t K,
+                       const himuon_ns_params& p, const StepArgs& st, size_t chunk_bytes,
+                       cudaStream_t stream) {
+  const int n = static_cast<int>(descs.size());
+  if (T < 1) return fail(HIMUON_ERR_INVALID_ARG, "T must be >= 1");
+  if (K < 0 || K > kMaxK) return fail(HIMUON_ERR_INVALID_ARG, "K must be in [0, 64]");
+
+  // ---- tile list and the per-tile byte bound used for chunking
+  int64_t total = 0, maxside = 0;
+  std::vector<int64_t> tile_bytes(n);
+  for (int i = 0; i < n; ++i) {
+    MatDesc& d = descs[i];
+    d.tiles_w = static_cast<int32_t>(cdiv(d.W, T));
+    const int64_t nt = cdiv(d.H, T) * d.tiles_w;
+    if (nt > (1LL << 31) - 1) return fail(HIMUON_ERR_INVALID_ARG, "too many tiles in one matrix");
+    d.ntiles = static_cast<int32_t>(nt);
+    d.tile_start = total;
+    total += nt;
+    maxside = std::max<int64_t>(maxside, std::max(d.H, d.W));
+    int64_t per = esize((d.flags & F_IN_FP32) ? HIMUON_FP32 : HIMUON_BF16);
+    if (st.enabled) per += ((d.flags & F_M_BF16) ? 2 : 4) + ((d.flags & F_OUT_FP32) ? 4 : 2);
+    tile_bytes[i] = std::min<int64_t>(T, d.H) * std::min<int64_t>(T, d.W) * per;
+  }
+
+  const bool fp32 = p.path == HIMUON_PATH_FP32;
+  const bool full = T >= maxside;  // one tile per matrix: the full-matrix map
+  if (!fp32 && T != 128) {
+    return fail(HIMUON_ERR_UNSUPPORTED,
+                "tensor path: T = " + std::to_string(T) +
+                    (full ? " (full-matrix)" : "") + " is not implemented in this build; "
+                    "use T = 128 or the fp32 path");
+  }
+
+  // ---- per-matrix norm partials
+  std::vector<int64_t> part_start(n + 1, 0);
+  for (int i = 0; i < n; ++i) part_start[i + 1] = part_start[i] + cdiv(descs[i].H, NORM_ROWS_PER_PART);
+  const int64_t nparts = (p.norm == HIMUON_NORM_MATRIX) ? part_start[n] : 0;
+
+  // ---- workspace: [descs | part_start | partials]
+  const size_t off_desc = 0;
+  const size_t off_part = (sizeof(MatDesc) * n + 255) & ~size_t(255);
+  const size_t off_partials = (off_part + sizeof(int64_t) * (n + 1) + 255) & ~size_t(255);
+  const size_t ws_need = off_partials + sizeof(float) * std::max<int64_t>(nparts, 1);
+  himuon_status s = grow(&h->ws, &h->ws_bytes, ws_need, stream, "workspace");
+  if (s != HIMUON_OK) return s;
+  h->host.assign(off_partials, 0);
+  std::memcpy(h->host.data() + off_desc, descs.data(), sizeof(MatDesc) * n);
+  std::memcpy(h->host.data() + off_part, part_start.data(), sizeof(int64_t) * (n + 1));
+  unsigned char* ws = static_cast<unsigned char*>(h->ws);
+  // Pageable source: the copy is staged before cudaMemcpyAsync returns, so the
+  // host buffer may be reused by the next call right away.
+  cudaError_t e = cudaMemcpyAsync(ws, h->host.data(), off_partials, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+  MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + off_desc);
+  const int64_t* d_part = reinterpret_cast<const int64_t*>(ws + off_part);
+  float* d_partials = reinterpret_cast<float*>(ws + off_partials);
+
+  NSArgs ns{p.a, p.b, p.c, p.eps, p.norm, K, T};
+  if (p.norm == HIMUON_NORM_MATRIX) {
+    e = launch_matrix_norms(d_descs, n, d_part, nparts, d_partials, p.eps, st, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "matrix norm launch");
+    h->launches += 2;
+  }
+
+  // ---- chunks: consecutive tile ranges whose input bytes stay within budget
+  std::vector<std::pair<int64_t, int64_t>> chunks;
+  if (chunk_bytes == 0) {
+    chunks.emplace_back(0, total);
+  } else {
+    int64_t begin = 0, used = 0;
+    for (int i = 0; i < n; ++i) {
+      int64_t left = descs[i].ntiles, pos = descs[i].tile_start;
+      const int64_t b = tile_bytes[i];
+      while (left > 0) {
+        const int64_t cap = static_cast<int64_t>(chunk_bytes) - used;
+        int64_t k = std::min<int64_t>(left, cap >= b ? cap / b : 0);
+        if (k == 0) {
+          if (pos > begin) {                      // close the current chunk
+            chunks.emplace_back(begin, pos);
+            begin = pos;
+            used = 0;
+            continue;
+          }
+          k = 1;                                  // one tile above the budget
+        }
+        pos += k;
+        left -= k;
+        used += k * b;
+      }
+    }
+    if (total > begin) chunks.emplace_back(begin, total);
+  }
+
+  if (fp32) {
+    const int P = static_cast<int>(std::min<int64_t>(T, maxside));
+    const size_t per_tile = size_t(3) * P * P * sizeof(float);
+    int64_t nb = std::max<int64_t>(1, static_cast<int64_t>(kFp32ScratchCap / per_tile));
+    nb = std::min<int64_t>(nb, 65535);
+    int64_t biggest = 0;
+    for (auto& c : chunks) biggest = std::max(biggest, c.second - c.first);
+    nb = std::min(nb, biggest);
+    void* scr = h->scratch;
+    s = grow(&scr, &h->scratch_bytes, per_tile * nb, stream, "fp32 scratch");
+    h->scratch = static_cast<float*>(scr);
+    if (s != HIMUON_OK) return s;
+    for (auto& c : chunks) {
+      e = launch_ns_fp32(d_descs, n, c.first, c.second, T, P, ns, st, h->scratch, nb, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "fp32 path launch");
+      const int64_t subs = (c.second - c.first + nb - 1) / nb;
+      h->launches += subs * (2 + (ns.norm != HIMUON_NORM_NONE ? 1 : 0) + 3 * K);
+    }
+    return HIMUON_OK;
+  }
+
+  for (auto& c : chunks) {
+    e = launch_ns_tc128(d_descs, n, c.first, c.second, ns, st, h->wait_ns, h->d_err, h->num_sms,
+                        stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
+    h->launches += 1;
+  }
+  return HIMUON_OK;
+}
+
+int32_t in_flags(int32_t gtype, const void* g, int64_t ldg) {
+  int32_t f = 0;
+  if (gtype == HIMUON_FP32) f |= F_IN_FP32;
+  if (aligned16(g, ldg, gtype)) f |= F_IN_VEC;
+  return f;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t himuon_launch_count(const himuon_handle* h) { return h ? h->launches : 0; }
+
+int32_t himuon_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* himuon_last_error_string(void) { return g_last_error.c_str(); }
+
+void himuon_default_ns_params(himuon_ns_params* p) {
+  if (!p) return;
+  p->a = 3.4445f;
+  p->b = -4.7750f;
+  p->c = 2.0315f;
+  p->norm = HIMUON_NORM_TILE;
+  p->eps = 1e-7f;
+  p->path = HIMUON_PATH_AUTO;
+}
+
+double himuon_ns_flops(int64_t H, int64_t W, int32_t T, int32_t K) {
+  if (H < 0 || W < 0 || T < 0 || K < 0) return 0.0;
+  return 6.0 * static_cast<double>(H) * static_cast<double>(W) * static_cast<double>(T) *
+         static_cast<double>(K);
+}
+
+int32_t himuon_schedule_tile(const int64_t* start_step, const int32_t* tile, int32_t n_points,
+                             int64_t step) {
+  if (!start_step || !tile || n_points < 1) return 0;
+  for (int32_t i = 1; i < n_points; ++i)
+    if (start_step[i] <= start_step[i - 1]) return 0;
+  int32_t t = tile[0];
+  for (int32_t i = 0; i < n_points; ++i)
+    if (start_step[i] <= step) t = tile[i];
+  return t;
+}
+
+himuon_status himuon_create(himuon_handle** out_handle) {
+  if (!out_handle) return fail(HIMUON_ERR_INVALID_ARG, "out_handle is NULL");
+  *out_handle = nullptr;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(HIMUON_ERR_NO_DEVICE, std::string("no CUDA device: ") + cudaGetErrorString(e));
+  }
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3))
+    return fail(HIMUON_ERR_NO_DEVICE, "libhimuon is built for sm_103a (B300); device is sm_" +
+                                          std::to_string(prop.major) + std::to_string(prop.minor));
+  himuon_handle* h = new himuon_handle();
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  e = cudaMalloc(&h->d_err, 256);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 256);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "error word allocation");
+  }
+  *out_handle = h;
+  return HIMUON_OK;
+}
+
+himuon_status himuon_destroy(himuon_handle* h) {
+  if (!h) return HIMUON_OK;
+  cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->scratch) cudaFree(h->scratch);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+  return HIMUON_OK;
+}
+
+himuon_status himuon_set_wait_limit(himuon_handle* h, uint64_t ns) {
+  if (!h) return fail(HIMUON_ERR_INVALID_ARG, "handle is NULL");
+  if (ns == 0) return fail(HIMUON_ERR_INVALID_ARG, "wait limit must be > 0");
+  h->wait_ns = ns;
+  return HIMUON_OK;
+}
+
+himuon_status himuon_device_error(himuon_handle* h, void* stream, int32_t* code) {
+  himuon_status s = check_handle(h);
+  if (s != HIMUON_OK) return s;
+  if (!code) return fail(HIMUON_ERR_INVALID_ARG, "code is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream sync");
+  int v = 0;
+  e = cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error word read");
+  e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "error word clear");
+  *code = v;
+  return HIMUON_OK;
+}
+
+himuon_status himuon_wait_selftest(himuon_handle* h, void* stream) {
+  himuon_status s = check_handle(h);
+  if (s != HIMUON_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_wait_selftest(h->wait_ns, h->d_err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test sync");
+  return HIMUON_OK;
+}
+
+himuon_status himuon_tiled_ns(himuon_handle* h, const void* G, int64_t H, int64_t W, int64_t ldg,
+                              int32_t gtype, int32_t T, int32_t K, const himuon_ns_params* params,
+                              void* out, int64_t ldo, int32_t otype, void* stream) {
+  himuon_matrix m;
+  m.g = G;
+  m.out = out;
+  m.H = H;
+  m.W = W;
+  m.ldg = ldg;
+  m.ldo = ldo;
+  m.gtype = gtype;
+  m.otype = otype;
+  return himuon_tiled_ns_batched(h, &m, 1, T, K, params, 0, stream);
+}
+
+himuon_status himuon_tiled_ns_batched(himuon_handle* h, const himuon_matrix* mats, int32_t n,
+                                      int32_t T, int32_t K, const himuon_ns_params* params,
+                                      size_t chunk_bytes, void* stream) {
+  himuon_status s = check_handle(h);
+  if (s != HIMUON_OK) return s;
+  if (!mats || n < 1) return fail(HIMUON_ERR_INVALID_ARG, "need at least one matrix");
+  himuon_ns_params p;
+  himuon_default_ns_params(&p);
+  if (params) p = *params;
+  if ((s = check_ns_params(p)) != HIMUON_OK) return s;
+  if (T < 1) return fail(HIMUON_ERR_INVALID_ARG, "T must be >= 1");
+  if (K < 0 || K > kMaxK) return fail(HIMUON_ERR_INVALID_ARG, "K must be in [0, 64]");
+  std::vector<MatDesc> descs(n);
+  for (int32_t i = 0; i < n; ++i) {
+    const himuon_matrix& m = mats[i];
+    const std::string tag = "matrix " + std::to_string(i);
+    if (!m.g || !m.out) return fail(HIMUON_ERR_INVALID_ARG, tag + ": NULL pointer");
+    if (!valid_dtype(m.gtype) || !valid_dtype(m.otype))
+      return fail(HIMUON_ERR_INVALID_ARG, tag + ": unknown dtype");
+    if ((s = check_shape(m.H, m.W, m.ldg, (tag + " input").c_str())) != HIMUON_OK) return s;
+    if ((s = check_shape(m.H, m.W, m.ldo, (tag + " output").c_str())) != HIMUON_OK) return s;
+    if (m.g != m.out && overlaps(m.g, m.H, m.W, m.ldg, m.gtype, m.out, m.ldo, m.otype))
+      return fail(HIMUON_ERR_INVALID_ARG, tag + ": output partially overlaps the input");
+    if (m.g == m.out && (m.ldg != m.ldo || m.gtype != m.otype))
+      return fail(HIMUON_ERR_INVALID_ARG, tag + ": in-place needs the same ld and dtype");
+    MatDesc d{};
+    d.in = m.g;
+    d.out = m.out;
+    d.mom = nullptr;
+    d.ld_in = m.ldg;
+    d.ld_out = m.ldo;
+    d.ld_mom = 0;
+    d.H = static_cast<int32_t>(m.H);
+    d.W = static_cast<int32_t>(m.W);
+    d.flags = in_flags(m.gtype, m.g, m.ldg);
+    if (m.otype == HIMUON_FP32) d.flags |= F_OUT_FP32;
+    if (aligned16(m.out, m.ldo, m.otype)) d.flags |= F_OUT_VEC;
+    d.upd_scale = 0.f;
+    d.norm_scale = 1.f;
+    descs[i] = d;
+  }
+  StepArgs st{0.f, 1.f, 0, 0};
+  return run_plan(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
+}
+
+himuon_status himuon_step(himuon_handle* h, const himuon_param* params, int32_t n, int32_t T,
+                          int32_t K, const himuon_ns_params* nsp, const himuon_step_params* step,
+                          size_t chunk_bytes, void* stream) {
+  himuon_status s = check_handle(h);
+  if (s != HIMUON_OK) return s;
+  if (!params || n < 1) return fail(HIMUON_ERR_INVALID_ARG, "need at least one parameter matrix");
+  if (!step) return fail(HIMUON_ERR_INVALID_ARG, "step params are NULL");
+  himuon_ns_params p;
+  himuon_default_ns_params(&p);
+  if (nsp) p = *nsp;
+  if ((s = check_ns_params(p)) != HIMUON_OK) return s;
+  if (T < 1) return fail(HIMUON_ERR_INVALID_ARG, "T must be >= 1");
+  if (K < 0 || K > kMaxK) return fail(HIMUON_ERR_INVALID_ARG, "K must be in [0, 64]");
+  if (!std::isfinite(step->lr) || !std::isfinite(step->mu) || !std::isfinite(step->weight_decay))
+    return fail(HIMUON_ERR_INVALID_ARG, "step params must be finite");
+  if (!(step->scale_mode == 0 || step->scale_mode == 1))
+    return fail(HIMUON_ERR_INVALID_ARG, "unknown scale mode");
+  std::vector<MatDesc> descs(n);
+  for (int32_t i = 0; i < n; ++i) {
+    const himuon_param& q = params[i];
+    const std::string tag = "param " + std::to_string(i);
+    if (!q.w || !q.g || !q.m) return fail(HIMUON_ERR_INVALID_ARG, tag + ": NULL pointer");
+    if (!valid_dtype(q.wtype) || !valid_dtype(q.gtype) || !valid_dtype(q.mtype))
+      return fail(HIMUON_ERR_INVALID_ARG, tag + ": unknown dtype");
+    if ((s = check_shape(q.H, q.W, q.ldw, (tag + " W").c_str())) != HIMUON_OK) return s;
+    if ((s = check_shape(q.H, q.W, q.ldg, (tag + " G").c_str())) != HIMUON_OK) return s;
+    if ((s = check_shape(q.H, q.W, q.ldm, (tag + " M").c_str())) != HIMUON_OK) return s;
+    if (overlaps(q.w, q.H, q.W, q.ldw, q.wtype, q.g, q.ldg, q.gtype) ||
+        overlaps(q.w, q.H, q.W, q.ldw, q.wtype, q.m, q.ldm, q.mtype) ||
+        overlaps(q.g, q.H, q.W, q.ldg, q.gtype, q.m, q.ldm, q.mtype))
+      return fail(HIMUON_ERR_INVALID_ARG, tag + ": W, G and M must not overlap");
+    MatDesc d{};
+    d.in = q.g;
+    d.out = q.w;
+    d.mom = q.m;
+    d.ld_in = q.ldg;
+    d.ld_out = q.ldw;
+    d.ld_mom = q.ldm;
+    d.H = static_cast<int32_t>(q.H);
+    d.W = static_cast<int32_t>(q.W);
+    d.flags = in_flags(q.gtype, q.g, q.ldg);
+    if (q.wtype == HIMUON_FP32) d.flags |= F_OUT_FP32;
+    if (aligned16(q.w, q.ldw, q.wtype)) d.flags |= F_OUT_VEC;
+    if (q.mtype == HIMUON_BF16) d.flags |= F_M_BF16;
+    if (aligned16(q.m, q.ldm, q.mtype)) d.flags |= F_M_VEC;
+    const double sc = step->scale_mode == 0
+                          ? std::sqrt(std::max(1.0, static_cast<double>(q.H) / static_cast<double>(q.W)))
+                          : 1.0;
+    d.upd_scale = static_cast<float>(static_cast<double>(step->lr) * sc);
+    d.norm_scale = 1.f;
+    descs[i] = d;
+  }
+  StepArgs st;
+  st.mu = step->mu;
+  st.wd_factor = static_cast<float>(1.0 - static_cast<double>(step->lr) * step->weight_decay);
+  st.nesterov = step->nesterov ? 1 : 0;
+  st.enabled = 1;
+  return run_plan(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

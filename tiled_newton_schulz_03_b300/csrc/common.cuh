@@ -1,0 +1,72 @@
+// Internal definitions shared by the kernels and the host planner of libhimuon.
+//
+// A launch drains a flat list of tiles taken from several matrices (cross-layer
+// batching). Each matrix is described by one MatDesc in device memory; tile
+// `t` of the launch belongs to the matrix whose [tile_start, tile_start + ntiles)
+// range contains it.
+#pragma once
+
+#include <cstdint>
+
+namespace himuon {
+
+// dtype codes, equal to himuon_dtype
+enum : int32_t { DT_BF16 = 0, DT_FP32 = 1 };
+
+// MatDesc.flags bits
+enum : int32_t {
+  F_IN_FP32 = 1 << 0,     // input (G) is fp32 (else bf16)
+  F_OUT_FP32 = 1 << 1,    // output (out, or W for a step) is fp32 (else bf16)
+  F_M_BF16 = 1 << 2,      // momentum buffer is bf16 (else fp32)
+  F_IN_VEC = 1 << 3,      // 16-byte vector loads of the input are legal
+  F_OUT_VEC = 1 << 4,     // 16-byte vector stores/loads of out / W are legal
+  F_M_VEC = 1 << 5,       // 16-byte vector access of M is legal
+};
+
+struct MatDesc {
+  const void* in;      // G
+  void* out;           // NS output, or W for a step
+  void* mom;           // momentum buffer (step only)
+  int64_t ld_in, ld_out, ld_mom;
+  int32_t H, W;
+  int32_t tiles_w;     // ceil(W / T)
+  int32_t ntiles;      // ceil(H / T) * tiles_w
+  int64_t tile_start;  // first tile of this matrix in the launch's flat list
+  int32_t flags;
+  float upd_scale;     // step: lr * s (s = per-matrix update scale)
+  float norm_scale;    // NORM_MATRIX: 1 / (||G||_F + eps), written on the device
+  float pad_[3];
+};
+static_assert(sizeof(MatDesc) == 96, "MatDesc layout");
+
+enum : int32_t { NORM_TILE = 0, NORM_MATRIX = 1, NORM_NONE = 2 };
+
+struct NSArgs {
+  float a, b, c, eps;
+  int32_t norm;
+  int32_t K;
+  int32_t T;
+};
+
+struct StepArgs {
+  float mu;
+  float wd_factor;     // 1 - lr * weight_decay
+  int32_t nesterov;
+  int32_t enabled;     // 0: plain NS launch
+};
+
+// Error codes written into the device error word (equal to himuon_status).
+enum : int32_t { DEV_ERR_TIMEOUT = 4 };
+
+// Tile -> matrix lookup by binary search over tile_start (n is small).
+__device__ __forceinline__ int find_matrix(const MatDesc* __restrict__ d, int n,
+                                           int64_t tile) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (d[mid].tile_start <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace himuon
