@@ -189,7 +189,8 @@ def test_step_matches_oracle(path):
         tol = TOL_BF16 if path == "tensor" else TOL_FP32
         bound = tol * np.linalg.norm(d_ref) + np.linalg.norm(np.abs(Wn) * 2.0 ** -8)
         assert np.linalg.norm(d_gpu - d_ref) <= bound
-        assert rel_fro(f64(Ws[i]), Wn) <= tol
+        # W itself is stored in bf16: per element at most 2^-9 relative rounding
+        assert rel_fro(f64(Ws[i]), Wn) <= tol + 2.0 ** -9
 
 
 def test_step_zero_lr_keeps_weights_and_updates_momentum():

@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   uint32_t phase = 0;
   const int K = ns.K;
+  // Part (a - d) of the a X term is moved into the bf16 operand C = B + (a - d) I,
+  // d = min(a, 1.5): the spectrum of B (about [-2.8, 0] for the quintic) is
+  // then centred on zero, which shrinks the bf16 rounding of C relative to the
+  // result a + B where a + b s^2 + c s^4 nearly cancels (rank-1 tiles).
+  const float shift = ns.a > 1.5f ? ns.a - 1.5f : 0.f;
 
   // Waits for the MMAs committed last; one thread polls (bounded), all sync.
   auto wait_mma = [&]() -> bool {
@@ -367,7 +372,11 @@ __global__ void __launch_bounds__(NTHR, 1)
         ptx::tmem_ld32_sync(t_acc_w + ch * 32, a2);
 #pragma unroll
         for (int j = 0; j < 32; ++j) av[j] = fmaf(ns.c, a2[j], ns.b * av[j]);
-        put_bf16_row32(sA, r, ch, av);   // B = b A + c A^2, in place of A
+        if (ch == warp) {                 // this row's diagonal element: + (a - d)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) av[j] += (j == lane) ? shift : 0.f;
+        }
+        put_bf16_row32(sA, r, ch, av);   // C = b A + c A^2 + (a - d) I, in place of A
       }
       sync_for_mma();
 
@@ -375,15 +384,16 @@ __global__ void __launch_bounds__(NTHR, 1)
       issue(sA, sX, true);
       if (!wait_mma()) goto teardown;
       {
-        const float sa = ns.a * (k == 0 ? s : 1.f);
         const float sb = (k == 0) ? s : 1.f;
         const bool last = (k + 1 == K);
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
-          float bx[32], xp[32];
+          float bx[32], xp[32], xb[32];
           ptx::tmem_ld32x2_sync(t_acc_w + ch * 32, bx, t_xf_w + ch * 32, xp);
+          get_bf16_row32(sX, r, ch, xb);
+          // X' = C X_bf + a X - (a - d) X_bf  (= a X + B X_bf exactly)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) xp[j] = fmaf(sa, xp[j], sb * bx[j]);
+          for (int j = 0; j < 32; ++j) xp[j] = sb * fmaf(-shift, xb[j], fmaf(ns.a, xp[j], bx[j]));
           if (!last) {
             ptx::tmem_st32(t_xf_w + ch * 32, xp);
             put_bf16_row32(sX, r, ch, xp);
