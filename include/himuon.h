@@ -194,6 +194,52 @@ himuon_status himuon_set_wait_limit(himuon_handle* handle, uint64_t ns);
  */
 himuon_status himuon_wait_selftest(himuon_handle* handle, void* stream);
 
+/*
+ * Size of the fixed device scratch of himuon_tiled_ns_fp32_noalloc (bytes).
+ */
+#define HIMUON_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * Allocation-free variant of the fp32 validation path of himuon_tiled_ns.
+ * (The paper has no counterpart: this is a library convenience.)
+ *
+ * For callers that cannot call cudaMalloc: an application whose device memory
+ * is all reserved by its own allocator (for example a framework's caching
+ * allocator, or a process held to a fixed memory budget), or code that must
+ * not block, since cudaMalloc/cudaFree can synchronise the device. Such
+ * callers cannot create a handle, whose workspace is allocated on demand.
+ * This call takes no handle and allocates nothing -- no cudaMalloc, no
+ * cudaFree, no allocating library routine. Its scratch (the matrix descriptor,
+ * per-matrix norm partials and the fp32 tile buffers) is one file-scope
+ * device array of HIMUON_NOALLOC_SCRATCH_BYTES bytes, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments, layout and result are those of himuon_tiled_ns with
+ * params->path = HIMUON_PATH_FP32 (params->path is ignored here): G and out
+ * are caller-owned device pointers, H x W row-major with leading dimensions
+ * ldg / ldo; out may be G itself. The result equals that call's output.
+ * Limit: one zero-padded tile of side P = min(T, max(H, W)) needs 12 * P * P
+ * bytes (plus 4 bytes per 32 rows in NORM_MATRIX mode) and must fit in the
+ * array, i.e. P <= 1182; larger requests return HIMUON_ERR_INVALID_ARG with a
+ * message (himuon_last_error_string) naming the sizes, before any launch.
+ * Larger tile counts are processed in sub-batches that fit.
+ *
+ * Set-up: the first call on a device (that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before any stream capture on the device.
+ * Concurrency: all calls share the one array, whose contents persist from
+ * call to call (nothing in it needs clearing: each call writes every byte it
+ * reads before reading it). Calls whose work overlaps on the GPU -- on
+ * different streams, or from different host threads -- race on the array and
+ * give wrong results; issue them on one stream or serialise them.
+ * Asynchronous on `stream` like the other calls.
+ */
+himuon_status himuon_tiled_ns_fp32_noalloc(const void* G, int64_t H, int64_t W,
+                                           int64_t ldg, int32_t gtype, int32_t T,
+                                           int32_t K, const himuon_ns_params* params,
+                                           void* out, int64_t ldo, int32_t otype,
+                                           void* stream);
+
 /* Number of kernels this handle has launched so far (all calls, all paths). */
 int64_t himuon_launch_count(const himuon_handle* handle);
 

@@ -25,6 +25,7 @@ __all__ = [
     "QUINTIC", "HimuonError", "Handle", "library_path", "load_library", "tiled_ns",
     "tiled_ns_batched", "step", "ns_flops", "schedule_tile", "TSchedule",
     "device_error", "set_wait_limit", "wait_selftest", "EXPORTED_SYMBOLS", "default_handle",
+    "tiled_ns_fp32_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 QUINTIC = (3.4445, -4.7750, 2.0315)
@@ -38,7 +39,11 @@ EXPORTED_SYMBOLS = [
     "himuon_tiled_ns_batched", "himuon_step", "himuon_schedule_tile", "himuon_ns_flops",
     "himuon_device_error", "himuon_set_wait_limit", "himuon_wait_selftest",
     "himuon_last_error_string", "himuon_version", "himuon_launch_count",
+    "himuon_tiled_ns_fp32_noalloc",
 ]
+
+# Size of the fixed device scratch of himuon_tiled_ns_fp32_noalloc (HIMUON_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
            5: "NO_DEVICE", 6: "OUT_OF_MEMORY"}
@@ -116,6 +121,8 @@ def load_library():
             "himuon_last_error_string": (ctypes.c_char_p, []),
             "himuon_version": (I32, []),
             "himuon_launch_count": (I64, [P]),
+            "himuon_tiled_ns_fp32_noalloc": (I32, [P, I64, I64, I64, I32, I32, I32,
+                                                   ctypes.POINTER(NSParams), P, I64, I32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -217,6 +224,30 @@ def tiled_ns(G: torch.Tensor, T: int, K: int = 5, coeffs=QUINTIC, norm: str = "t
         _check(load_library().himuon_tiled_ns(h.ptr, g, H, W, ldg, gt, int(T), int(K),
                                               ctypes.byref(p), o, ldo, ot,
                                               _stream_ptr(stream, G.device)))
+    return out
+
+
+def tiled_ns_fp32_noalloc(G: torch.Tensor, T: int, K: int = 5, coeffs=QUINTIC,
+                          norm: str = "tile", eps: float = 1e-7, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """fp32 tiled NS of one matrix through the allocation-free entry point.
+
+    For callers that cannot let the library allocate device memory: no handle
+    is used and the library's scratch is its fixed device array. ``out`` must
+    be given (this wrapper does not allocate one either); it is returned.
+    Calls that overlap on the GPU share that array and must be serialised.
+    """
+    if out is None:
+        raise HimuonError(1, "out must be given (this call allocates nothing)")
+    g, H, W, ldg, gt = _mat_info(G, "G")
+    o, H2, W2, ldo, ot = _mat_info(out, "out")
+    if (H2, W2) != (H, W):
+        raise HimuonError(1, "out must have the shape of G")
+    p = _ns_params(coeffs, norm, eps, "fp32")
+    with torch.cuda.device(G.device):
+        _check(load_library().himuon_tiled_ns_fp32_noalloc(g, H, W, ldg, gt, int(T), int(K),
+                                                           ctypes.byref(p), o, ldo, ot,
+                                                           _stream_ptr(stream, G.device)))
     return out
 
 

@@ -83,6 +83,11 @@ himuon_status check_shape(int64_t H, int64_t W, int64_t ld, const char* what) {
 
 }  // namespace
 
+namespace himuon {
+// Lets the other translation units of the library set the last-error string.
+void record_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace himuon
+
 struct himuon_handle {
   int device = -1;
   int num_sms = 0;

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <string>
 
 #include "common.cuh"
 
@@ -37,5 +38,8 @@ constexpr int NORM_ROWS_PER_PART = 32;
 // One CTA waits on an mbarrier that nothing arrives on, for wait_ns, then
 // records a time-out in *err and returns (aux_kernels.cu).
 cudaError_t launch_wait_selftest(uint64_t wait_ns, int* err, cudaStream_t stream);
+
+// Sets the message himuon_last_error_string() returns on this host thread (api.cu).
+void record_last_error(const std::string& msg);
 
 }  // namespace himuon
