@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 METRIC = "HiMuon step ms & tiled-NS TFLOP/s vs bf16 tensor peak (8B layer set, T=128, K=5)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNEL = "ns_tc128_kernel"
+KERNEL = "ns_tc_kernel"
 
 WORKLOADS = {
     # name: (shapes fn, rank of the synthetic gradients, T, K, chunk bytes)

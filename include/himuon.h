@@ -68,7 +68,10 @@ typedef enum {
 } himuon_norm;
 
 typedef enum {
-  HIMUON_PATH_AUTO = 0,    /* bf16 tensor-core path (tcgen05) */
+  HIMUON_PATH_AUTO = 0,    /* bf16 tensor-core path (tcgen05); matrices with
+                              min(H, W) <= 2 or fewer than 4096 elements run on
+                              the fp32 path (too few elements for the bf16
+                              rounding to average out) */
   HIMUON_PATH_TENSOR = 1,  /* same, requested explicitly */
   HIMUON_PATH_FP32 = 2     /* fp32 validation path (CUDA cores, fp32 FMA) */
 } himuon_path;

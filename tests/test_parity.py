@@ -43,8 +43,9 @@ def built():
 
 # ---------------------------------------------------------------- one matrix
 
-@pytest.mark.parametrize("T,path,tol", [(128, "tensor", TOL_BF16), (64, "fp32", TOL_FP32),
-                                        (128, "fp32", TOL_FP32), (32, "fp32", TOL_FP32)])
+@pytest.mark.parametrize("T,path,tol", [(128, "tensor", TOL_BF16), (64, "tensor", TOL_BF16),
+                                        (64, "fp32", TOL_FP32), (128, "fp32", TOL_FP32),
+                                        (32, "fp32", TOL_FP32)])
 def test_gaussian_fp32_256x512(T, path, tol):
     G = synth.gaussian(256, 512, seed=0)            # fp32, N(0, 1)
     out = hm.tiled_ns(G.cuda(), T, 5, path=path, out_dtype=torch.float32)
@@ -55,10 +56,11 @@ def test_gaussian_fp32_256x512(T, path, tol):
 @pytest.mark.parametrize("H,W", [(300, 530), (128, 128), (1, 1), (1, 300), (257, 3),
                                  (129, 255), (768, 3072)])
 @pytest.mark.parametrize("path", ["tensor", "fp32"])
-def test_lowrank_bf16_ragged(H, W, path):
+@pytest.mark.parametrize("T", [128, 64])
+def test_lowrank_bf16_ragged(H, W, path, T):
     G = synth.lowrank_noise(H, W, seed=H * 7 + W)
-    out = hm.tiled_ns(G.cuda(), 128, 5, path=path, out_dtype=torch.float32)
-    want = oracle.tiled_ns(f64(G), 128, 5)
+    out = hm.tiled_ns(G.cuda(), T, 5, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
     assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
 
 
@@ -242,7 +244,7 @@ def test_bad_arguments_raise_without_launch():
     with pytest.raises(hm.HimuonError):
         hm.tiled_ns(G, 128, 5, out=G[:, :3])
     with pytest.raises(hm.HimuonError) as e:
-        hm.tiled_ns(G, 96, 5)                        # no tensor kernel for T = 96
+        hm.tiled_ns(G, 96, 5, path="tensor")         # no tensor kernel for T = 96
     assert e.value.status_name == "UNSUPPORTED"
     big = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(hm.HimuonError):               # partial overlap of out and G

@@ -7,6 +7,7 @@
 // of any number of matrices form one work list (cross-layer batching) that can
 // be cut anywhere into launches (memory-bounded chunking), and T may differ from
 // call to call (runtime tile-size schedules) -- sentence 6.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -121,6 +122,45 @@ himuon_status grow(void** buf, size_t* have, size_t need, cudaStream_t stream, c
   return HIMUON_OK;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D tiled map of an H x W row-major matrix (leading dimension ld elements),
+// box of box_w columns x box_h rows, 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, int64_t H, int64_t W, int64_t ld, bool fp32,
+              int box_w, int box_h) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const int64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * es)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_w), static_cast<cuuint32_t>(box_h)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 himuon_status check_handle(himuon_handle* h) {
   if (!h) return fail(HIMUON_ERR_INVALID_ARG, "handle is NULL");
   int dev = -1;
@@ -158,11 +198,25 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
 
   const bool fp32 = p.path == HIMUON_PATH_FP32;
   const bool full = T >= maxside;  // one tile per matrix: the full-matrix map
-  if (!fp32 && T != 128) {
+  if (!fp32 && T != 128 && T != 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
                     (full ? " (full-matrix)" : "") + " is not implemented in this build; "
-                    "use T = 128 or the fp32 path");
+                    "use T = 64 or 128, or the fp32 path");
+  }
+
+  // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
+  // step bf16 G and fp32 M); other matrices are staged with plain loads.
+  std::vector<CUtensorMap> maps(fp32 ? 0 : 2 * static_cast<size_t>(n));
+  for (int i = 0; i < n && !fp32; ++i) {
+    MatDesc& d = descs[i];
+    const bool in32 = d.flags & F_IN_FP32;
+    bool ok = (d.flags & F_IN_VEC) != 0;
+    if (st.enabled) ok = ok && !in32 && (d.flags & F_M_VEC) && !(d.flags & F_M_BF16);
+    std::memset(&maps[2 * i], 0, 2 * sizeof(CUtensorMap));
+    if (ok) ok = make_map(&maps[2 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
+    if (ok && st.enabled) ok = make_map(&maps[2 * i + 1], d.mom, d.H, d.W, d.ld_mom, true, 32, T);
+    if (ok) d.flags |= F_TMA;
   }
 
   // ---- per-matrix norm partials
@@ -170,16 +224,19 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   for (int i = 0; i < n; ++i) part_start[i + 1] = part_start[i] + cdiv(descs[i].H, NORM_ROWS_PER_PART);
   const int64_t nparts = (p.norm == HIMUON_NORM_MATRIX) ? part_start[n] : 0;
 
-  // ---- workspace: [descs | part_start | partials]
+  // ---- workspace: [descs | part_start | tensor maps | partials]
   const size_t off_desc = 0;
   const size_t off_part = (sizeof(MatDesc) * n + 255) & ~size_t(255);
-  const size_t off_partials = (off_part + sizeof(int64_t) * (n + 1) + 255) & ~size_t(255);
+  const size_t off_maps = (off_part + sizeof(int64_t) * (n + 1) + 255) & ~size_t(255);
+  const size_t off_partials = (off_maps + sizeof(CUtensorMap) * maps.size() + 255) & ~size_t(255);
   const size_t ws_need = off_partials + sizeof(float) * std::max<int64_t>(nparts, 1);
   himuon_status s = grow(&h->ws, &h->ws_bytes, ws_need, stream, "workspace");
   if (s != HIMUON_OK) return s;
   h->host.assign(off_partials, 0);
   std::memcpy(h->host.data() + off_desc, descs.data(), sizeof(MatDesc) * n);
   std::memcpy(h->host.data() + off_part, part_start.data(), sizeof(int64_t) * (n + 1));
+  if (!maps.empty())
+    std::memcpy(h->host.data() + off_maps, maps.data(), sizeof(CUtensorMap) * maps.size());
   unsigned char* ws = static_cast<unsigned char*>(h->ws);
   // Pageable source: the copy is staged before cudaMemcpyAsync returns, so the
   // host buffer may be reused by the next call right away.
@@ -187,6 +244,7 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
   MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + off_desc);
   const int64_t* d_part = reinterpret_cast<const int64_t*>(ws + off_part);
+  const void* d_maps = ws + off_maps;
   float* d_partials = reinterpret_cast<float*>(ws + off_partials);
 
   NSArgs ns{p.a, p.b, p.c, p.eps, p.norm, K, T};
@@ -247,10 +305,38 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   }
 
   for (auto& c : chunks) {
-    e = launch_ns_tc128(d_descs, n, c.first, c.second, ns, st, h->wait_ns, h->d_err, h->num_sms,
-                        stream);
+    e = launch_ns_tc(d_descs, d_maps, n, c.first, c.second, ns, st, h->wait_ns, h->d_err,
+                     h->num_sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
     h->launches += 1;
+  }
+  return HIMUON_OK;
+}
+
+// Under HIMUON_PATH_AUTO, matrices this small or thin run on the fp32 path:
+// with so few elements the bf16 rounding of the tensor path does not average
+// out (errors of several percent on rank-1 matrices of a few elements), and a
+// 128-row tensor-core product would be almost all padding anyway.
+bool needs_fp32(const MatDesc& d) {
+  return std::min(d.H, d.W) <= 2 || static_cast<int64_t>(d.H) * d.W < 4096;
+}
+
+// Runs the plan, with the small matrices of an AUTO-path request split off to
+// the fp32 path (two plans on the same stream, so they run one after another).
+himuon_status run_auto(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T, int32_t K,
+                       const himuon_ns_params& p, const StepArgs& st, size_t chunk_bytes,
+                       cudaStream_t stream) {
+  if (p.path != HIMUON_PATH_AUTO) return run_plan(h, descs, T, K, p, st, chunk_bytes, stream);
+  std::vector<MatDesc> big, small;
+  for (const MatDesc& d : descs) (needs_fp32(d) ? small : big).push_back(d);
+  if (!big.empty()) {
+    himuon_status s = run_plan(h, big, T, K, p, st, chunk_bytes, stream);
+    if (s != HIMUON_OK) return s;
+  }
+  if (!small.empty()) {
+    himuon_ns_params q = p;
+    q.path = HIMUON_PATH_FP32;
+    return run_plan(h, small, T, K, q, st, chunk_bytes, stream);
   }
   return HIMUON_OK;
 }
@@ -428,7 +514,7 @@ himuon_status himuon_tiled_ns_batched(himuon_handle* h, const himuon_matrix* mat
     descs[i] = d;
   }
   StepArgs st{0.f, 1.f, 0, 0};
-  return run_plan(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
+  return run_auto(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
 }
 
 himuon_status himuon_step(himuon_handle* h, const himuon_param* params, int32_t n, int32_t T,
@@ -488,7 +574,7 @@ himuon_status himuon_step(himuon_handle* h, const himuon_param* params, int32_t 
   st.wd_factor = static_cast<float>(1.0 - static_cast<double>(step->lr) * step->weight_decay);
   st.nesterov = step->nesterov ? 1 : 0;
   st.enabled = 1;
-  return run_plan(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
+  return run_auto(h, descs, T, K, p, st, chunk_bytes, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -21,6 +21,7 @@ enum : int32_t {
   F_IN_VEC = 1 << 3,      // 16-byte vector loads of the input are legal
   F_OUT_VEC = 1 << 4,     // 16-byte vector stores/loads of out / W are legal
   F_M_VEC = 1 << 5,       // 16-byte vector access of M is legal
+  F_TMA = 1 << 6,         // tensor maps of G (and M for a step) exist: TMA staging
 };
 
 struct MatDesc {

@@ -11,13 +11,13 @@
 
 namespace himuon {
 
-// Tensor-core tiled NS, T = 128, tile resident in SMEM/TMEM (ns_tc128.cu).
-// descs: device array of ndesc MatDesc; tiles [tile_begin, tile_end) of the
-// flat tile list are processed. st.enabled selects the fused HiMuon step.
-cudaError_t launch_ns_tc128(const MatDesc* descs, int ndesc, int64_t tile_begin, int64_t tile_end,
-                            const NSArgs& ns, const StepArgs& st, uint64_t wait_ns, int* err,
-                            int num_sms, cudaStream_t stream);
-int tc128_smem_bytes();
+// Tensor-core tiled NS, T in {64, 128} (ns_tc.cu). descs: device array of ndesc
+// MatDesc; maps: device array of 2 * ndesc CUtensorMap (G, M), 64-byte aligned,
+// valid for matrices flagged F_TMA; tiles [tile_begin, tile_end) of the flat
+// tile list are processed. st.enabled selects the fused HiMuon step.
+cudaError_t launch_ns_tc(const MatDesc* descs, const void* maps, int ndesc, int64_t tile_begin,
+                         int64_t tile_end, const NSArgs& ns, const StepArgs& st, uint64_t wait_ns,
+                         int* err, int num_sms, cudaStream_t stream);
 
 // fp32 validation path (ns_fp32.cu): tiles (cut at multiples of T) padded to
 // P x P (P = min(T, largest matrix side)) in a scratch buffer of 3 * nb * P * P

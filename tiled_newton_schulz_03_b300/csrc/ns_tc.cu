@@ -1,0 +1,860 @@
+// Tiled Newton-Schulz on tcgen05 tensor cores, T in {64, 128}: warp-specialised,
+// two tile slots per SM, TMA-fed.
+//
+// Method ("Hierarchical Muon: Tiled Newton-Schulz Updates for Efficient Muon
+// Optimization", abstract, sentences 3-5): every T x T tile X of a
+// momentum-gradient matrix is normalised and iterated K times with
+//   A = X X^T,  B = b A + c A^2,  X <- a X + B X,
+// independently of every other tile. The three products per step are dense
+// T x T x T contractions, run here as tcgen05.mma (bf16 operands, fp32
+// accumulation in tensor memory).
+//
+// CTA (one per SM, 20 warps = 5 per scheduler, so 96 registers per thread):
+//   warps 0-3   loader: brings the next stage's G (and M) into a staging buffer
+//               with TMA (plain loads for layouts TMA cannot describe), applies
+//               momentum (M <- mu M + G, stored back with TMA) and computes the
+//               per-tile sums of squares for the normalisation. Warp 0 also
+//               allocates and frees tensor memory.
+//   warps 4-11  slot 0, warps 12-19 slot 1 (8 warps each: lane quarter =
+//               warp % 4, column half = (warp - first) / 4). A slot's warps run
+//               the epilogue of each product and its first thread issues the
+//               slot's next product.
+// The two slots hold two independent stages; while the tensor core runs one
+// slot's product, the other slot's warps run their epilogue, so the serial
+// chain of a tile's 3K products never leaves the tensor pipe idle for long.
+//
+// A stage is 128 rows: one 128 x 128 tile, or two 64 x 64 tiles stacked
+// vertically (T = 64). With stacked tiles, tile t's products use the whole
+// 128-row stack as the A operand and tile t's rows as the B operand; only the
+// accumulator lanes of tile t are kept (the others hold unused cross products).
+//
+// Per slot, on chip for all K steps:
+//   sX  (smem 32 KB)   X in bf16, 128-byte swizzled, 128-byte rows: operand of
+//                      X X^T (K-major) and of C X (MN-major).
+//   sC  (smem 32 KB)   A in bf16 (operand of A A), then C in bf16 (operand of C X).
+//   R_A (TMEM, 128 columns)  accumulator of X X^T, then of (b/c) A_bf + A_bf A_bf + (e/c) I.
+//   R_X (TMEM, 128 columns)  fp32 iterate: holds a X - e X_bf before C X_bf is
+//                      accumulated onto it, X' afterwards.
+// Rounding: with e = a - min(a, 1.5) and C = B + e I,
+//   X' = C X_bf + (a X - e X_bf) = a X + B X_bf      (exact identity),
+// so X keeps fp32 precision in the a X term, and the bf16 operand C has its
+// spectrum (about [-2.8, 0] for the quintic's B) centred near zero, which keeps
+// its rounding small where a + B nearly cancels (rank-1 tiles).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace himuon {
+namespace {
+
+constexpr int NWARPS = 20;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int SLOT_WARP0 = 4;
+constexpr int LOADER_THREADS = 128;
+constexpr int SLOT_THREADS = 256;
+
+// shared memory (offsets from the 1024-byte aligned base)
+// slot s: sX at s * 64 KB, sC at s * 64 KB + 32 KB
+__host__ __device__ constexpr uint32_t sm_x(int s) { return static_cast<uint32_t>(s) * 65536u; }
+__host__ __device__ constexpr uint32_t sm_c(int s) { return static_cast<uint32_t>(s) * 65536u + 32768u; }
+constexpr uint32_t SM_S0 = 131072;  // 64 KB: fp32 tile, 4 blocks of 128 rows x 32 columns
+constexpr uint32_t SM_S1 = 196608;  // 32 KB: bf16 tile, 2 blocks of 128 rows x 64 columns
+constexpr uint32_t SM_END = 229376;
+constexpr uint32_t SMEM_DYN = SM_END + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+
+// how a sub-tile sits in the staging buffer
+enum : int { FMT_U32 = 0, FMT_G16 = 1, FMT_G16M32 = 2 };
+
+struct Ctl {
+  uint64_t acc_full[2];   // tensor core -> slot: the slot's last product is complete
+  uint64_t st_full[2];    // loader -> slot s: staging holds this slot's next stage
+  uint64_t st_empty;      // slot -> loader: staging has been read
+  uint64_t st_loaded;     // TMA -> loader: staging bytes have landed
+  uint64_t drain[2];      // slot issuer: all its MMAs complete (abort path)
+  uint32_t tmem_base;
+  int abort_flag;
+  float part[4];          // per loader warp: sum of squares of its 32 rows
+  int info_mi[4], info_i0[4], info_j0[4], info_h[4], info_w[4], info_fmt[4];
+  float info_s[4];
+};
+
+// ------------------------------------------------------------------ layouts
+// bf16 tile: element (r, c) in block c / 64, 16-byte chunk ((c % 64) / 8) ^ (r % 8).
+__device__ __forceinline__ uint32_t bf_off(int r, int c8) {   // c8 = c / 8
+  return static_cast<uint32_t>((c8 >> 3) * 16384 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
+}
+// fp32 tile: element (r, c) in block c / 32, 16-byte chunk ((c % 32) / 4) ^ (r % 8).
+__device__ __forceinline__ uint32_t f32_off(int r, int c4) {  // c4 = c / 4
+  return static_cast<uint32_t>((c4 >> 3) * 16384 + r * 128 + (((c4 & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ packed fp32 pairs
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// v[j] *= s for 32 values, in pairs
+__device__ __forceinline__ void scale32(float (&v)[32], float s) {
+  const uint64_t ss = pk2(s, s);
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    uint64_t x = mul2(pk2(v[j], v[j + 1]), ss);
+    upk2(x, v[j], v[j + 1]);
+  }
+}
+
+// 32 fp32 -> 16 packed bf16x2 -> 4 x 16-byte chunks of a bf16 tile row
+__device__ __forceinline__ void st_bf16_32(uint32_t tile, int r, int c, const float (&v)[32],
+                                           uint32_t (&pkd)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    ptx::st_shared_v4(tile + bf_off(r, (c >> 3) + q), pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2],
+                      pkd[4 * q + 3]);
+}
+
+__device__ __forceinline__ void ld_bf16_32(uint32_t tile, int r, int c, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = ptx::ld_shared_v4(tile + bf_off(r, (c >> 3) + q));
+    v[8 * q + 0] = ptx::bf16lo(u.x); v[8 * q + 1] = ptx::bf16hi(u.x);
+    v[8 * q + 2] = ptx::bf16lo(u.y); v[8 * q + 3] = ptx::bf16hi(u.y);
+    v[8 * q + 4] = ptx::bf16lo(u.z); v[8 * q + 5] = ptx::bf16hi(u.z);
+    v[8 * q + 6] = ptx::bf16lo(u.w); v[8 * q + 7] = ptx::bf16hi(u.w);
+  }
+}
+
+__device__ __forceinline__ void ld_f32_32(uint32_t tile, int r, int c, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint4 u = ptx::ld_shared_v4(tile + f32_off(r, (c >> 2) + q));
+    v[4 * q + 0] = __uint_as_float(u.x); v[4 * q + 1] = __uint_as_float(u.y);
+    v[4 * q + 2] = __uint_as_float(u.z); v[4 * q + 3] = __uint_as_float(u.w);
+  }
+}
+
+__device__ __forceinline__ void st_f32_32(uint32_t tile, int r, int c, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    ptx::st_shared_v4(tile + f32_off(r, (c >> 2) + q), __float_as_uint(v[4 * q]),
+                      __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                      __float_as_uint(v[4 * q + 3]));
+}
+
+// single elements of the staging tiles (for tiles processed transposed)
+__device__ __forceinline__ float f32_at(uint32_t tile, int r, int c) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(tile + f32_off(r, c >> 2) + (c & 3) * 4));
+  return v;
+}
+__device__ __forceinline__ float bf16_at(uint32_t tile, int r, int c) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(tile + bf_off(r, c >> 3) + (c & 7) * 2));
+  return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+
+// ------------------------------------------------------------------ global row segments
+// 32 elements from column c0 of a row, n of them valid (0..32); vector access
+// when all 32 are valid and the row allows 16-byte access.
+__device__ __forceinline__ void gload32(const void* rowp, int c0, int n, bool fp32, bool vec,
+                                        float (&v)[32]) {
+  if (n >= 32 && vec) {
+    if (fp32) {
+      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(rowp) + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f = p[q];
+        v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+      }
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(rowp) + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = p[q];
+        v[8 * q + 0] = ptx::bf16lo(u.x); v[8 * q + 1] = ptx::bf16hi(u.x);
+        v[8 * q + 2] = ptx::bf16lo(u.y); v[8 * q + 3] = ptx::bf16hi(u.y);
+        v[8 * q + 4] = ptx::bf16lo(u.z); v[8 * q + 5] = ptx::bf16hi(u.z);
+        v[8 * q + 6] = ptx::bf16lo(u.w); v[8 * q + 7] = ptx::bf16hi(u.w);
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float x = 0.f;
+    if (j < n)
+      x = fp32 ? static_cast<const float*>(rowp)[c0 + j]
+               : __bfloat162float(static_cast<const __nv_bfloat16*>(rowp)[c0 + j]);
+    v[j] = x;
+  }
+}
+
+__device__ __forceinline__ void gstore32(void* rowp, int c0, int n, bool fp32, bool vec,
+                                         const float (&v)[32]) {
+  if (n >= 32 && vec) {
+    if (fp32) {
+      float4* p = reinterpret_cast<float4*>(static_cast<float*>(rowp) + c0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(rowp) + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        p[q] = make_uint4(ptx::pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
+                          ptx::pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                          ptx::pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                          ptx::pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j < n) {
+      if (fp32) static_cast<float*>(rowp)[c0 + j] = v[j];
+      else static_cast<__nv_bfloat16*>(rowp)[c0 + j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ char* gptr(const void* base, int64_t ld, int64_t row, int64_t col,
+                                      bool fp32) {
+  return const_cast<char*>(static_cast<const char*>(base)) + (row * ld + col) * (fp32 ? 4 : 2);
+}
+
+// ------------------------------------------------------------------ bounded waits
+// Waits for the phase of `bar` with the given parity. Gives up once the CTA
+// has aborted or after limit_ns (then records the time-out and aborts the CTA).
+// After an abort every wait returns at once, so all roles run to the end.
+__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                         volatile int* abort_flag, int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  uint32_t n = 0;
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0) {
+      if (*abort_flag) return;
+      if (ptx::globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+        return;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void tensormap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+// Tile of a launch's flat list: matrix, origin and valid extent.
+struct TileRef {
+  int mi, i0, j0, h, w;
+};
+template <int T>
+__device__ __forceinline__ TileRef tile_ref(const MatDesc* descs, int ndesc, int64_t tile) {
+  TileRef t;
+  t.mi = find_matrix(descs, ndesc, tile);
+  const MatDesc& d = descs[t.mi];
+  const int64_t lt = tile - d.tile_start;
+  t.i0 = static_cast<int>(lt / d.tiles_w) * T;
+  t.j0 = static_cast<int>(lt % d.tiles_w) * T;
+  t.h = min(T, d.H - t.i0);
+  t.w = min(T, d.W - t.j0);
+  return t;
+}
+
+template <bool STEP>
+__device__ __forceinline__ int tile_format(int flags) {
+  if (!(flags & F_TMA)) return FMT_U32;
+  if (STEP) return FMT_G16M32;
+  return (flags & F_IN_FP32) ? FMT_U32 : FMT_G16;
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int T, bool STEP>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    ns_tc_kernel(const MatDesc* __restrict__ descs, const CUtensorMap* __restrict__ maps, int ndesc,
+                 int64_t tile_begin, int64_t tile_end, NSArgs ns, StepArgs st, uint64_t wait_ns,
+                 int* __restrict__ err) {
+  constexpr int TPS = 128 / T;          // tiles per stage (stacked)
+  constexpr int HALF = T / 2;           // columns per epilogue thread
+  constexpr int NCH = HALF / 32;        // 32-column chunks per epilogue thread
+  static_assert(T == 64 || T == 128, "T");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Ctl ctl;
+
+  const uint32_t sbase = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &ctl.abort_flag;
+
+  const uint32_t b_acc[2] = {ptx::smem_u32(&ctl.acc_full[0]), ptx::smem_u32(&ctl.acc_full[1])};
+  const uint32_t b_full[2] = {ptx::smem_u32(&ctl.st_full[0]), ptx::smem_u32(&ctl.st_full[1])};
+  const uint32_t b_empty = ptx::smem_u32(&ctl.st_empty);
+  const uint32_t b_loaded = ptx::smem_u32(&ctl.st_loaded);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(b_acc[s], 1);
+      ptx::mbar_init(b_full[s], 4);
+      ptx::mbar_init(ptx::smem_u32(&ctl.drain[s]), 1);
+    }
+    ptx::mbar_init(b_empty, 8);
+    ptx::mbar_init(b_loaded, 1);
+    ptx::fence_mbar_init();
+    ctl.abort_flag = 0;
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tbase = ctl.tmem_base;
+
+  const int K = ns.K;
+  const int64_t stride_tiles = static_cast<int64_t>(gridDim.x) * TPS;
+  const int64_t first_tile = tile_begin + static_cast<int64_t>(blockIdx.x) * TPS;
+  // e = a - min(a, 1.5): part of a I moved into the bf16 operand C = B + e I
+  const float e = ns.a > 1.5f ? ns.a - 1.5f : 0.f;
+  const bool has_c = ns.c != 0.f;
+
+  if (warp < 4) {
+    // =============================================================== loader
+    const int r = threadIdx.x;              // stage row
+    const int t = r / T, rl = r % T;        // sub-tile and row within it
+    int last_mi = -1;
+    uint32_t ld_phase = 0;
+    int64_t g = 0;
+    for (int64_t base = first_tile; base < tile_end; base += stride_tiles, ++g) {
+      wait_bar(b_empty, static_cast<uint32_t>((g & 1) ^ 1), wait_ns, abort_flag, err);
+      if (STEP) {
+        // the previous stage's M stores must have read the staging buffer
+        if (r == 0) ptx::bulk_wait_read0();
+        named_sync(1, LOADER_THREADS);
+      }
+
+      // which sub-tiles are valid, and where they come from
+      TileRef ref[TPS];
+      int fmt[TPS];
+      bool any_tma = false;
+#pragma unroll
+      for (int u = 0; u < TPS; ++u) {
+        const int64_t tile = base + u;
+        if (tile < tile_end) {
+          ref[u] = tile_ref<T>(descs, ndesc, tile);
+          fmt[u] = tile_format<STEP>(descs[ref[u].mi].flags);
+          any_tma |= (descs[ref[u].mi].flags & F_TMA) != 0;
+        } else {
+          ref[u] = TileRef{-1, 0, 0, 0, 0};
+          fmt[u] = FMT_U32;
+        }
+      }
+
+      if (any_tma) {
+        if (r == 0 && !*abort_flag) {
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int u = 0; u < TPS; ++u) {
+            if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
+            bytes += (fmt[u] == FMT_U32 ? 4u : 2u) * T * T;   // G: fp32 or bf16
+            if (STEP) bytes += 4u * T * T;
+          }
+          ptx::mbar_arrive_expect_tx(b_loaded, bytes);
+#pragma unroll
+          for (int u = 0; u < TPS; ++u) {
+            if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
+            const CUtensorMap* mg = maps + 2 * ref[u].mi;
+            if (ref[u].mi != last_mi) {
+              tensormap_acquire(mg);
+              if (STEP) tensormap_acquire(mg + 1);
+              last_mi = ref[u].mi;
+            }
+            const uint32_t row_off = static_cast<uint32_t>(u * T * 128);
+            if (fmt[u] == FMT_G16 || fmt[u] == FMT_G16M32) {
+              for (int b = 0; b < T / 64; ++b)
+                ptx::tma_load_2d(sbase + SM_S1 + b * 16384 + row_off, mg, ref[u].j0 + 64 * b,
+                                 ref[u].i0, b_loaded);
+            } else {   // fp32 G into the fp32 tile
+              for (int b = 0; b < T / 32; ++b)
+                ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + row_off, mg, ref[u].j0 + 32 * b,
+                                 ref[u].i0, b_loaded);
+            }
+            if (STEP) {
+              for (int b = 0; b < T / 32; ++b)
+                ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + row_off, mg + 1, ref[u].j0 + 32 * b,
+                                 ref[u].i0, b_loaded);
+            }
+          }
+        }
+        wait_bar(b_loaded, ld_phase, wait_ns, abort_flag, err);
+        ld_phase ^= 1u;
+      }
+
+      // ---- row pass: this thread's row r of sub-tile t
+      float ss = 0.f;
+      const TileRef& me = ref[t];
+      if (me.mi < 0) {
+        float z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+        for (int c = 0; c < T; c += 32) st_f32_32(sbase + SM_S0, r, c, z);
+      } else if (fmt[t] == FMT_G16M32) {
+#pragma unroll 1
+        for (int c = 0; c < T; c += 32) {
+          float gv[32], mv[32];
+          ld_bf16_32(sbase + SM_S1, r, c, gv);
+          ld_f32_32(sbase + SM_S0, r, c, mv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float mn = fmaf(st.mu, mv[j], gv[j]);
+            mv[j] = mn;
+            const float u = st.nesterov ? fmaf(st.mu, mn, gv[j]) : mn;
+            ss = fmaf(u, u, ss);
+          }
+          st_f32_32(sbase + SM_S0, r, c, mv);
+        }
+        ptx::fence_proxy_async_smem();      // M_new goes back to HBM through TMA
+      } else if (fmt[t] == FMT_G16 && (descs[me.mi].flags & F_TMA)) {
+#pragma unroll 1
+        for (int c = 0; c < T; c += 32) {
+          float gv[32];
+          ld_bf16_32(sbase + SM_S1, r, c, gv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(gv[j], gv[j], ss);
+        }
+      } else if (descs[me.mi].flags & F_TMA) {   // fp32 G already in the fp32 tile
+#pragma unroll 1
+        for (int c = 0; c < T; c += 32) {
+          float gv[32];
+          ld_f32_32(sbase + SM_S0, r, c, gv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(gv[j], gv[j], ss);
+        }
+      } else {
+        // plain loads (any alignment): U = G, or U from momentum; M written back here
+        const MatDesc& d = descs[me.mi];
+        const bool in32 = d.flags & F_IN_FP32;
+        const bool row_ok = rl < me.h;
+        const char* gp = row_ok ? gptr(d.in, d.ld_in, me.i0 + rl, me.j0, in32) : nullptr;
+        const bool m16 = d.flags & F_M_BF16;
+        char* mp = (STEP && row_ok) ? gptr(d.mom, d.ld_mom, me.i0 + rl, me.j0, !m16) : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < T; c += 32) {
+          const int n = row_ok ? max(0, min(32, me.w - c)) : 0;
+          float u[32];
+          gload32(gp, c, n, in32, d.flags & F_IN_VEC, u);
+          if (STEP) {
+            float mv[32];
+            gload32(mp, c, n, !m16, d.flags & F_M_VEC, mv);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float mn = fmaf(st.mu, mv[j], u[j]);
+              mv[j] = mn;
+              u[j] = st.nesterov ? fmaf(st.mu, mn, u[j]) : mn;
+            }
+            if (n > 0) gstore32(mp, c, n, !m16, d.flags & F_M_VEC, mv);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(u[j], u[j], ss);
+          st_f32_32(sbase + SM_S0, r, c, u);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) ctl.part[warp] = ss;
+      named_sync(1, LOADER_THREADS);
+
+      if (r == 0) {
+        if (STEP && !*abort_flag) {
+          bool stored = false;
+#pragma unroll
+          for (int u = 0; u < TPS; ++u) {
+            if (ref[u].mi < 0 || fmt[u] != FMT_G16M32) continue;
+            const CUtensorMap* mm = maps + 2 * ref[u].mi + 1;
+            for (int b = 0; b < T / 32; ++b) {
+              if (32 * b >= ref[u].w) break;       // box wholly right of the matrix
+              ptx::tma_store_2d(mm, sbase + SM_S0 + b * 16384 + u * T * 128, ref[u].j0 + 32 * b,
+                                ref[u].i0);
+            }
+            stored = true;
+          }
+          if (stored) ptx::bulk_commit();
+        }
+#pragma unroll
+        for (int u = 0; u < TPS; ++u) {
+          float s = 1.f;
+          if (ref[u].mi >= 0) {
+            if (ns.norm == NORM_TILE) {
+              float acc = 0.f;
+              for (int w = u * (T / 32); w < (u + 1) * (T / 32); ++w) acc += ctl.part[w];
+              s = 1.f / (sqrtf(acc) + ns.eps);
+            } else if (ns.norm == NORM_MATRIX) {
+              s = descs[ref[u].mi].norm_scale;
+            }
+          }
+          ctl.info_mi[u] = ref[u].mi;
+          ctl.info_i0[u] = ref[u].i0;
+          ctl.info_j0[u] = ref[u].j0;
+          ctl.info_h[u] = ref[u].h;
+          ctl.info_w[u] = ref[u].w;
+          ctl.info_fmt[u] = fmt[u];
+          ctl.info_s[u] = s;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_full[g & 1]);
+    }
+    if (r == 0) ptx::bulk_wait0();
+  } else {
+    // =============================================================== epilogue slots
+    const int s = (warp - SLOT_WARP0) / 8;
+    const int ws = (warp - SLOT_WARP0) % 8;
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int hh = ws >> 2;                 // column half
+    const int r = 32 * q + lane;            // stage row = TMEM lane
+    const int t = r / T, rl = r % T;
+    const int cbase = hh * HALF;            // first tile column of this thread
+    const uint32_t sx = sbase + sm_x(s), sc = sbase + sm_c(s);
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t t_a = tbase + lane_off + 256u * s + t * T;           // R_A of my tile
+    const uint32_t t_x = tbase + lane_off + 256u * s + 128u + t * T;    // R_X of my tile
+    const float bc = has_c ? ns.b / ns.c : 0.f;
+    const float ec = has_c ? e / ns.c : 0.f;
+    uint32_t acc_ph = 0;
+    const bool issuer = (ws == 0 && lane == 0);
+    bool issued = false;
+
+    // Product p of this slot (0: X X^T -> R_A; 1: A A onto R_A; 2: C X onto R_X),
+    // one 128 x T x T MMA per stacked tile, completion signalled on acc_full[s].
+    auto issue = [&](int p) {
+      if (!issuer || *abort_flag) return;
+      constexpr uint32_t IDESC_KK = ptx::idesc_bf16_f32(128, T, false, false);
+      constexpr uint32_t IDESC_KM = ptx::idesc_bf16_f32(128, T, false, true);
+      ptx::tc_fence_after();
+      const uint32_t dcol = tbase + 256u * s + (p == 2 ? 128u : 0u);
+      const uint32_t a_base = (p == 0) ? sx : sc;
+#pragma unroll
+      for (int u = 0; u < TPS; ++u) {
+#pragma unroll
+        for (int kk = 0; kk < T / 16; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(a_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          uint64_t bd;
+          if (p == 2) {
+            bd = ptx::sdesc_sw128(sx + (u * T + 16 * kk) * 128, 16384, 1024);
+          } else {
+            bd = ptx::sdesc_sw128(a_base + u * T * 128 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          }
+          const uint32_t accum = (p != 0 || kk > 0) ? 1u : 0u;
+          ptx::umma_bf16(dcol + u * T, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, accum);
+        }
+      }
+      ptx::umma_commit(b_acc[s]);
+      issued = true;
+    };
+
+    // End of the slot's work on a row segment: store the result, or apply the update.
+    // A transposed tile (tr) holds the result's column rl in the thread's row.
+    auto emit = [&](const MatDesc& d, int i0, int j0, int h, int w, bool tr, int c,
+                    float (&o)[32]) {
+      if (tr) {
+        if (rl >= w) return;
+        const bool out32 = d.flags & F_OUT_FP32;
+        const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale);
+        const uint64_t wdf = pk2(st.wd_factor, st.wd_factor);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float w0 = 0.f, w1 = 0.f;
+          char* p0 = gptr(d.out, d.ld_out, i0 + c + j, j0 + rl, out32);
+          char* p1 = gptr(d.out, d.ld_out, i0 + c + j + 1, j0 + rl, out32);
+          const bool ok0 = c + j < h, ok1 = c + j + 1 < h;
+          if (STEP) {
+            if (ok0) w0 = out32 ? *reinterpret_cast<float*>(p0) : __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(p0));
+            if (ok1) w1 = out32 ? *reinterpret_cast<float*>(p1) : __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(p1));
+            upk2(fma2(nls, pk2(o[j], o[j + 1]), mul2(wdf, pk2(w0, w1))), w0, w1);
+          } else {
+            w0 = o[j];
+            w1 = o[j + 1];
+          }
+          if (ok0) {
+            if (out32) *reinterpret_cast<float*>(p0) = w0;
+            else *reinterpret_cast<__nv_bfloat16*>(p0) = __float2bfloat16_rn(w0);
+          }
+          if (ok1) {
+            if (out32) *reinterpret_cast<float*>(p1) = w1;
+            else *reinterpret_cast<__nv_bfloat16*>(p1) = __float2bfloat16_rn(w1);
+          }
+        }
+        return;
+      }
+      if (rl >= h) return;
+      const int n = max(0, min(32, w - c));
+      if (n == 0) return;
+      const bool out32 = d.flags & F_OUT_FP32;
+      char* op = gptr(d.out, d.ld_out, i0 + rl, j0, out32);
+      if (STEP) {
+        float wv[32];
+        gload32(op, c, n, out32, d.flags & F_OUT_VEC, wv);
+        const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale);
+        const uint64_t wdf = pk2(st.wd_factor, st.wd_factor);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          uint64_t x = fma2(nls, pk2(o[j], o[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1])));
+          upk2(x, wv[j], wv[j + 1]);
+        }
+        gstore32(op, c, n, out32, d.flags & F_OUT_VEC, wv);
+      } else {
+        gstore32(op, c, n, out32, d.flags & F_OUT_VEC, o);
+      }
+    };
+
+    // Operands written: make them visible to the tensor core, then the slot's
+    // first thread issues product p.
+    auto hand_over = [&](bool smem_written, bool tmem_written, int p) {
+      if (tmem_written) ptx::tmem_wait_st();
+      if (smem_written) ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      named_sync(2 + s, SLOT_THREADS);
+      issue(p);
+    };
+
+    int64_t g = s;
+    for (int64_t base = first_tile + s * stride_tiles; base < tile_end;
+         base += 2 * stride_tiles, g += 2) {
+      wait_bar(b_full[s], static_cast<uint32_t>((g >> 1) & 1), wait_ns, abort_flag, err);
+      const int mi = ctl.info_mi[t];
+      const int i0 = ctl.info_i0[t], j0 = ctl.info_j0[t];
+      const int th = ctl.info_h[t], tw = ctl.info_w[t];
+      const int fmt = ctl.info_fmt[t];
+      const float snorm = ctl.info_s[t];
+
+      // ---- prologue: staging -> sX = U_bf and R_X = s (a U - e U_bf). The input
+      // itself (exact for bf16 G) is the first step's operand; the normalisation
+      // factor s is applied to the first step's fp32 epilogue values instead, so
+      // that X_0 = s U is never rounded to bf16 a second time.
+      // A wide tile (fewer valid rows than columns) runs transposed: X^T has the
+      // same map (p(X)^T = p(X^T)), and with the short side as the Gram's side
+      // the bf16 rounding of X enters B X through a projection that averages
+      // it over the long side, instead of elementwise.
+      const bool tr = th < tw;
+#pragma unroll 1
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int c = cbase + 32 * ch;
+        float y[32];
+        if (tr) {
+          const int r0 = t * T + c;          // stage row of tile row c
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (fmt == FMT_G16) {
+              y[j] = bf16_at(sbase + SM_S1, r0 + j, rl);
+            } else if (fmt == FMT_G16M32) {
+              const float mv = f32_at(sbase + SM_S0, r0 + j, rl);
+              y[j] = st.nesterov ? fmaf(st.mu, mv, bf16_at(sbase + SM_S1, r0 + j, rl)) : mv;
+            } else {
+              y[j] = f32_at(sbase + SM_S0, r0 + j, rl);
+            }
+          }
+        } else if (fmt == FMT_G16) {
+          ld_bf16_32(sbase + SM_S1, r, c, y);
+        } else if (fmt == FMT_G16M32) {
+          float mv[32];
+          ld_bf16_32(sbase + SM_S1, r, c, y);
+          ld_f32_32(sbase + SM_S0, r, c, mv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] = st.nesterov ? fmaf(st.mu, mv[j], y[j]) : mv[j];
+        } else {
+          ld_f32_32(sbase + SM_S0, r, c, y);
+        }
+        if (K == 0) {
+          scale32(y, snorm);
+          if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, y);
+          continue;
+        }
+        uint32_t pkd[16];
+        st_bf16_32(sx, r, c, y, pkd);
+        const uint64_t a2 = pk2(snorm * ns.a, snorm * ns.a), ne2 = pk2(-snorm * e, -snorm * e);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          uint64_t x = fma2(a2, pk2(y[2 * j], y[2 * j + 1]),
+                            mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
+          upk2(x, y[2 * j], y[2 * j + 1]);
+        }
+        ptx::tmem_st32(t_x + c, y);
+      }
+      // staging consumed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_empty);
+      if (K == 0) continue;
+      hand_over(true, true, 0);            // -> X X^T
+
+#pragma unroll 1
+      const float s2 = snorm * snorm;
+      for (int k = 0; k < K; ++k) {
+        // ---- E1: A = X X^T in R_A
+        wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
+        acc_ph ^= 1u;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int c = cbase + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_a + c, v);
+          uint32_t pkd[16];
+          if (has_c) {
+            if (k == 0) scale32(v, s2);              // A = s^2 U_bf U_bf^T
+            st_bf16_32(sc, r, c, v, pkd);            // A_bf
+            // pre-init (b/c) A_bf + (e/c) I: the b A term takes the same rounded
+            // A as the A A product, so B is evaluated exactly at A_bf and the
+            // rounding enters through dB/dA = b + 2 c A, which is small where
+            // the two terms nearly cancel, instead of through 2 c A alone.
+            const uint64_t bc2 = pk2(bc, bc);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint64_t x = mul2(bc2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j])));
+              upk2(x, v[2 * j], v[2 * j + 1]);
+            }
+            if ((rl >> 5) == (c >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? ec : 0.f;
+            }
+            ptx::tmem_st32(t_a + c, v);
+          } else {
+            // C = b A + e I; on the first step s C, as the operand there is U_bf
+            scale32(v, k == 0 ? ns.b * s2 * snorm : ns.b);
+            const float dg = k == 0 ? e * snorm : e;
+            if ((rl >> 5) == (c >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? dg : 0.f;
+            }
+            st_bf16_32(sc, r, c, v, pkd);
+          }
+        }
+        hand_over(true, has_c, has_c ? 1 : 2);   // -> A A (or C X)
+
+        if (has_c) {
+          // ---- E2: R_A = (b/c) A + A A + (e/c) I  ->  C = c R_A
+          wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
+          acc_ph ^= 1u;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < NCH; ++ch) {
+            const int c = cbase + 32 * ch;
+            float v[32];
+            ptx::tmem_ld32_sync(t_a + c, v);
+            scale32(v, k == 0 ? ns.c * snorm : ns.c);   // first step: s C (operand U_bf)
+            uint32_t pkd[16];
+            st_bf16_32(sc, r, c, v, pkd);
+          }
+          hand_over(true, false, 2);       // -> C X
+        }
+
+        // ---- E3: R_X = X'
+        wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
+        acc_ph ^= 1u;
+        ptx::tc_fence_after();
+        const bool last = (k + 1 == K);
+#pragma unroll 1
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int c = cbase + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_x + c, v);
+          if (last) {
+            if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, v);
+          } else {
+            uint32_t pkd[16];
+            st_bf16_32(sx, r, c, v, pkd);
+            const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
+                                mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
+              upk2(x, v[2 * j], v[2 * j + 1]);
+            }
+            ptx::tmem_st32(t_x + c, v);
+          }
+        }
+        if (!last) hand_over(true, true, 0);   // -> next X X^T
+      }
+    }
+
+    if (issued && *abort_flag) {
+      // let every MMA this slot issued finish before tensor memory is released
+      const uint32_t bd = ptx::smem_u32(&ctl.drain[s]);
+      ptx::umma_commit(bd);
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(bd, 0) && ptx::globaltimer() - t0 < wait_ns) {
+      }
+    }
+  }
+
+  // =============================================================== teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+template <int T, bool STEP>
+cudaError_t launch_t(const MatDesc* descs, const CUtensorMap* maps, int ndesc, int64_t tile_begin,
+                     int64_t tile_end, const NSArgs& ns, const StepArgs& st, uint64_t wait_ns,
+                     int* err, int num_sms, cudaStream_t stream) {
+  constexpr int TPS = 128 / T;
+  const int64_t stages = (tile_end - tile_begin + TPS - 1) / TPS;
+  const int grid = static_cast<int>(std::min<int64_t>(stages, num_sms));
+  cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<T, STEP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+  if (e != cudaSuccess) return e;
+  ns_tc_kernel<T, STEP><<<grid, NTHREADS, SMEM_DYN, stream>>>(descs, maps, ndesc, tile_begin,
+                                                              tile_end, ns, st, wait_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ns_tc(const MatDesc* descs, const void* maps, int ndesc, int64_t tile_begin,
+                         int64_t tile_end, const NSArgs& ns, const StepArgs& st, uint64_t wait_ns,
+                         int* err, int num_sms, cudaStream_t stream) {
+  if (tile_end <= tile_begin) return cudaSuccess;
+  const CUtensorMap* m = static_cast<const CUtensorMap*>(maps);
+  if (ns.T == 128)
+    return st.enabled ? launch_t<128, true>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream)
+                      : launch_t<128, false>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream);
+  if (ns.T == 64)
+    return st.enabled ? launch_t<64, true>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream)
+                      : launch_t<64, false>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace himuon
