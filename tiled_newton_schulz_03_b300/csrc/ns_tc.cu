@@ -32,7 +32,7 @@
 //   sX  (smem 32 KB)   X in bf16, 128-byte swizzled, 128-byte rows: operand of
 //                      X X^T (K-major) and of C X (MN-major).
 //   sC  (smem 32 KB)   A in bf16 (operand of A A), then C in bf16 (operand of C X).
-//   R_A (TMEM, 128 columns)  accumulator of X X^T, then of (b/c) A_bf + A_bf A_bf + (e/c) I.
+//   R_A (TMEM, 128 columns)  accumulator of X X^T, then of A_bf A_bf.
 //   R_X (TMEM, 128 columns)  fp32 iterate: holds a X - e X_bf before C X_bf is
 //                      accumulated onto it, X' afterwards.
 // Rounding: with e = a - min(a, 1.5) and C = B + e I,
@@ -78,7 +78,7 @@ struct Ctl {
   uint64_t drain[2];      // slot issuer: all its MMAs complete (abort path)
   uint32_t tmem_base;
   int abort_flag;
-  float part[4];          // per loader warp: sum of squares of its 32 rows
+  float part[2][8];       // per slot warp: sum of squares of its row segments
   int info_mi[4], info_i0[4], info_j0[4], info_h[4], info_w[4], info_fmt[4];
   float info_s[4];
 };
@@ -173,6 +173,10 @@ __device__ __forceinline__ float bf16_at(uint32_t tile, int r, int c) {
   return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
 
+__device__ __forceinline__ void f32_put(uint32_t tile, int r, int c, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(tile + f32_off(r, c >> 2) + (c & 3) * 4), "f"(v) : "memory");
+}
+
 // ------------------------------------------------------------------ global row segments
 // 32 elements from column c0 of a row, n of them valid (0..32); vector access
 // when all 32 are valid and the row allows 16-byte access.
@@ -245,19 +249,31 @@ __device__ __forceinline__ char* gptr(const void* base, int64_t ld, int64_t row,
 // Waits for the phase of `bar` with the given parity. Gives up once the CTA
 // has aborted or after limit_ns (then records the time-out and aborts the CTA).
 // After an abort every wait returns at once, so all roles run to the end.
+// try_wait with a suspend-time hint: the waiting thread sleeps until the phase
+// completes or about 20 us pass, instead of spinning on the issue slots that
+// the epilogue warps of its scheduler need.
+__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                          volatile int* abort_flag, int* err) {
   if (ptx::mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = ptx::globaltimer();
-  uint32_t n = 0;
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if ((++n & 63u) == 0) {
-      if (*abort_flag) return;
-      if (ptx::globaltimer() - t0 > limit_ns) {
-        *abort_flag = 1;
-        atomicCAS(err, 0, DEV_ERR_TIMEOUT);
-        return;
-      }
+  while (!try_wait_sleep(bar, parity)) {
+    if (*abort_flag) return;
+    if (ptx::globaltimer() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+      return;
     }
   }
 }
@@ -325,10 +341,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(b_acc[s], 1);
-      ptx::mbar_init(b_full[s], 4);
+      ptx::mbar_init(b_full[s], 1);
       ptx::mbar_init(ptx::smem_u32(&ctl.drain[s]), 1);
     }
-    ptx::mbar_init(b_empty, 8);
+    ptx::mbar_init(b_empty, 1);
     ptx::mbar_init(b_loaded, 1);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
@@ -355,14 +371,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int t = r / T, rl = r % T;        // sub-tile and row within it
     int last_mi = -1;
     uint32_t ld_phase = 0;
+    // TMA-staged momentum of the stage last handed to a slot: the slot writes
+    // M <- mu M + G into the staging buffer; once it has released the buffer,
+    // thread 0 stores it to HBM and waits until the store has read it.
+    int pend_mi[TPS], pend_i0[TPS], pend_j0[TPS], pend_w[TPS];
+#pragma unroll
+    for (int u = 0; u < TPS; ++u) pend_mi[u] = -1;
+    auto store_prev = [&]() {
+      bool stored = false;
+#pragma unroll
+      for (int u = 0; u < TPS; ++u) {
+        if (pend_mi[u] < 0) continue;
+        if (!*abort_flag) {
+          const CUtensorMap* mm = maps + 2 * pend_mi[u] + 1;
+          for (int b = 0; b < T / 32; ++b) {
+            if (32 * b >= pend_w[u]) break;     // box wholly right of the matrix
+            ptx::tma_store_2d(mm, sbase + SM_S0 + b * 16384 + u * T * 128, pend_j0[u] + 32 * b,
+                              pend_i0[u]);
+          }
+          stored = true;
+        }
+        pend_mi[u] = -1;
+      }
+      if (stored) {
+        ptx::bulk_commit();
+        ptx::bulk_wait_read0();
+      }
+    };
     int64_t g = 0;
     for (int64_t base = first_tile; base < tile_end; base += stride_tiles, ++g) {
-      wait_bar(b_empty, static_cast<uint32_t>((g & 1) ^ 1), wait_ns, abort_flag, err);
-      if (STEP) {
-        // the previous stage's M stores must have read the staging buffer
-        if (r == 0) ptx::bulk_wait_read0();
-        named_sync(1, LOADER_THREADS);
-      }
+      // staging free (the slot that read it has also finished its M stores)
+      if (r == 0) wait_bar(b_empty, static_cast<uint32_t>((g & 1) ^ 1), wait_ns, abort_flag, err);
+      named_sync(1, LOADER_THREADS);
 
       // which sub-tiles are valid, and where they come from
       TileRef ref[TPS];
@@ -381,88 +421,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
 
-      if (any_tma) {
-        if (r == 0 && !*abort_flag) {
-          uint32_t bytes = 0;
+      if (any_tma && r == 0 && !*abort_flag) {
+        uint32_t bytes = 0;
 #pragma unroll
-          for (int u = 0; u < TPS; ++u) {
-            if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
-            bytes += (fmt[u] == FMT_U32 ? 4u : 2u) * T * T;   // G: fp32 or bf16
-            if (STEP) bytes += 4u * T * T;
+        for (int u = 0; u < TPS; ++u) {
+          if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
+          bytes += (fmt[u] == FMT_U32 ? 4u : 2u) * T * T;   // G: fp32 or bf16
+          if (STEP) bytes += 4u * T * T;
+        }
+        ptx::mbar_arrive_expect_tx(b_loaded, bytes);
+#pragma unroll
+        for (int u = 0; u < TPS; ++u) {      // G first: its buffer holds nothing to store
+          if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
+          const CUtensorMap* mg = maps + 2 * ref[u].mi;
+          if (ref[u].mi != last_mi) {
+            tensormap_acquire(mg);
+            if (STEP) tensormap_acquire(mg + 1);
+            last_mi = ref[u].mi;
           }
-          ptx::mbar_arrive_expect_tx(b_loaded, bytes);
-#pragma unroll
-          for (int u = 0; u < TPS; ++u) {
-            if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
-            const CUtensorMap* mg = maps + 2 * ref[u].mi;
-            if (ref[u].mi != last_mi) {
-              tensormap_acquire(mg);
-              if (STEP) tensormap_acquire(mg + 1);
-              last_mi = ref[u].mi;
-            }
-            const uint32_t row_off = static_cast<uint32_t>(u * T * 128);
-            if (fmt[u] == FMT_G16 || fmt[u] == FMT_G16M32) {
-              for (int b = 0; b < T / 64; ++b)
-                ptx::tma_load_2d(sbase + SM_S1 + b * 16384 + row_off, mg, ref[u].j0 + 64 * b,
-                                 ref[u].i0, b_loaded);
-            } else {   // fp32 G into the fp32 tile
-              for (int b = 0; b < T / 32; ++b)
-                ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + row_off, mg, ref[u].j0 + 32 * b,
-                                 ref[u].i0, b_loaded);
-            }
-            if (STEP) {
-              for (int b = 0; b < T / 32; ++b)
-                ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + row_off, mg + 1, ref[u].j0 + 32 * b,
-                                 ref[u].i0, b_loaded);
-            }
+          const uint32_t row_off = static_cast<uint32_t>(u * T * 128);
+          if (fmt[u] == FMT_G16 || fmt[u] == FMT_G16M32) {
+            for (int b = 0; b < T / 64; ++b)
+              ptx::tma_load_2d(sbase + SM_S1 + b * 16384 + row_off, mg, ref[u].j0 + 64 * b,
+                               ref[u].i0, b_loaded);
+          } else {   // fp32 G into the fp32 tile
+            for (int b = 0; b < T / 32; ++b)
+              ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + row_off, mg, ref[u].j0 + 32 * b,
+                               ref[u].i0, b_loaded);
           }
         }
-        wait_bar(b_loaded, ld_phase, wait_ns, abort_flag, err);
-        ld_phase ^= 1u;
+        if (STEP) {
+          store_prev();                       // previous stage's M, then its buffer is free
+#pragma unroll
+          for (int u = 0; u < TPS; ++u) {
+            if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
+            const CUtensorMap* mm = maps + 2 * ref[u].mi + 1;
+            for (int b = 0; b < T / 32; ++b)
+              ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + u * T * 128, mm, ref[u].j0 + 32 * b,
+                               ref[u].i0, b_loaded);
+          }
+        }
+      } else if (STEP && r == 0) {
+        store_prev();
       }
+      named_sync(1, LOADER_THREADS);         // plain rows below overwrite the M buffer
 
-      // ---- row pass: this thread's row r of sub-tile t
-      float ss = 0.f;
+      // ---- rows TMA does not bring: plain loads (any alignment) into the fp32
+      // tile as U, momentum applied and M written back here; zeros for a stage's
+      // missing tiles.
       const TileRef& me = ref[t];
       if (me.mi < 0) {
         float z[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0.f;
         for (int c = 0; c < T; c += 32) st_f32_32(sbase + SM_S0, r, c, z);
-      } else if (fmt[t] == FMT_G16M32) {
-#pragma unroll 1
-        for (int c = 0; c < T; c += 32) {
-          float gv[32], mv[32];
-          ld_bf16_32(sbase + SM_S1, r, c, gv);
-          ld_f32_32(sbase + SM_S0, r, c, mv);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float mn = fmaf(st.mu, mv[j], gv[j]);
-            mv[j] = mn;
-            const float u = st.nesterov ? fmaf(st.mu, mn, gv[j]) : mn;
-            ss = fmaf(u, u, ss);
-          }
-          st_f32_32(sbase + SM_S0, r, c, mv);
-        }
-        ptx::fence_proxy_async_smem();      // M_new goes back to HBM through TMA
-      } else if (fmt[t] == FMT_G16 && (descs[me.mi].flags & F_TMA)) {
-#pragma unroll 1
-        for (int c = 0; c < T; c += 32) {
-          float gv[32];
-          ld_bf16_32(sbase + SM_S1, r, c, gv);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ss = fmaf(gv[j], gv[j], ss);
-        }
-      } else if (descs[me.mi].flags & F_TMA) {   // fp32 G already in the fp32 tile
-#pragma unroll 1
-        for (int c = 0; c < T; c += 32) {
-          float gv[32];
-          ld_f32_32(sbase + SM_S0, r, c, gv);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ss = fmaf(gv[j], gv[j], ss);
-        }
-      } else {
-        // plain loads (any alignment): U = G, or U from momentum; M written back here
+      } else if (!(descs[me.mi].flags & F_TMA)) {
         const MatDesc& d = descs[me.mi];
         const bool in32 = d.flags & F_IN_FP32;
         const bool row_ok = rl < me.h;
@@ -485,57 +498,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (n > 0) gstore32(mp, c, n, !m16, d.flags & F_M_VEC, mv);
           }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ss = fmaf(u[j], u[j], ss);
           st_f32_32(sbase + SM_S0, r, c, u);
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) ctl.part[warp] = ss;
+      if (any_tma) {
+        if (r == 0) wait_bar(b_loaded, ld_phase, wait_ns, abort_flag, err);
+        ld_phase ^= 1u;
+      }
       named_sync(1, LOADER_THREADS);
 
       if (r == 0) {
-        if (STEP && !*abort_flag) {
-          bool stored = false;
-#pragma unroll
-          for (int u = 0; u < TPS; ++u) {
-            if (ref[u].mi < 0 || fmt[u] != FMT_G16M32) continue;
-            const CUtensorMap* mm = maps + 2 * ref[u].mi + 1;
-            for (int b = 0; b < T / 32; ++b) {
-              if (32 * b >= ref[u].w) break;       // box wholly right of the matrix
-              ptx::tma_store_2d(mm, sbase + SM_S0 + b * 16384 + u * T * 128, ref[u].j0 + 32 * b,
-                                ref[u].i0);
-            }
-            stored = true;
-          }
-          if (stored) ptx::bulk_commit();
-        }
 #pragma unroll
         for (int u = 0; u < TPS; ++u) {
-          float s = 1.f;
-          if (ref[u].mi >= 0) {
-            if (ns.norm == NORM_TILE) {
-              float acc = 0.f;
-              for (int w = u * (T / 32); w < (u + 1) * (T / 32); ++w) acc += ctl.part[w];
-              s = 1.f / (sqrtf(acc) + ns.eps);
-            } else if (ns.norm == NORM_MATRIX) {
-              s = descs[ref[u].mi].norm_scale;
-            }
-          }
           ctl.info_mi[u] = ref[u].mi;
           ctl.info_i0[u] = ref[u].i0;
           ctl.info_j0[u] = ref[u].j0;
           ctl.info_h[u] = ref[u].h;
           ctl.info_w[u] = ref[u].w;
           ctl.info_fmt[u] = fmt[u];
-          ctl.info_s[u] = s;
+          ctl.info_s[u] = (ref[u].mi >= 0 && ns.norm == NORM_MATRIX) ? descs[ref[u].mi].norm_scale : 1.f;
+          if (STEP && ref[u].mi >= 0 && fmt[u] == FMT_G16M32) {
+            pend_mi[u] = ref[u].mi;
+            pend_i0[u] = ref[u].i0;
+            pend_j0[u] = ref[u].j0;
+            pend_w[u] = ref[u].w;
+          }
         }
+        mbar_arrive(b_full[g & 1]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_full[g & 1]);
     }
-    if (r == 0) ptx::bulk_wait0();
+    if (STEP && r == 0) {
+      // the last stage's momentum: wait until its slot has released the buffer
+      wait_bar(b_empty, static_cast<uint32_t>((g & 1) ^ 1), wait_ns, abort_flag, err);
+      store_prev();
+      ptx::bulk_wait0();
+    }
   } else {
     // =============================================================== epilogue slots
     const int s = (warp - SLOT_WARP0) / 8;
@@ -549,10 +546,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t t_a = tbase + lane_off + 256u * s + t * T;           // R_A of my tile
     const uint32_t t_x = tbase + lane_off + 256u * s + 128u + t * T;    // R_X of my tile
-    const float bc = has_c ? ns.b / ns.c : 0.f;
-    const float ec = has_c ? e / ns.c : 0.f;
     uint32_t acc_ph = 0;
-    const bool issuer = (ws == 0 && lane == 0);
+    // the slot's polling and MMA-issuing thread, on a scheduler of its own
+    // (warp 0, the loader's, is on scheduler 0)
+    const int pw = 1 + s;
+    const bool issuer = (ws == pw && lane == 0);
     bool issued = false;
 
     // Product p of this slot (0: X X^T -> R_A; 1: A A onto R_A; 2: C X onto R_X),
@@ -575,7 +573,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           } else {
             bd = ptx::sdesc_sw128(a_base + u * T * 128 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
           }
-          const uint32_t accum = (p != 0 || kk > 0) ? 1u : 0u;
+          const uint32_t accum = (p == 2 || kk > 0) ? 1u : 0u;   // C X onto a X - e X_bf
           ptx::umma_bf16(dcol + u * T, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, accum);
         }
       }
@@ -648,61 +646,112 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       issue(p);
     };
 
+    // Waits for the slot's last product: one thread polls, the slot syncs
+    // (warps waiting at a barrier take no issue slots from the working ones).
+    auto wait_acc = [&]() {
+      if (issuer) wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
+      acc_ph ^= 1u;
+      named_sync(2 + s, SLOT_THREADS);
+      ptx::tc_fence_after();
+    };
+
+    // U for tile columns [c, c + 32) of this thread's row (of X^T for a
+    // transposed tile). For staged G and M (FMT_G16M32), `apply` performs the
+    // momentum update M <- mu M + G in the staging buffer, from where the loader
+    // stores M to HBM (each element is owned by one thread); without `apply`
+    // the staged M is already the updated one.
+    auto read_u = [&](int fmt, bool tr, int c, bool apply, float (&y)[32]) {
+      if (tr) {
+        const int r0 = t * T + c;            // stage row of tile row c
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (fmt == FMT_G16) {
+            y[j] = bf16_at(sbase + SM_S1, r0 + j, rl);
+          } else if (fmt == FMT_G16M32) {
+            const float gv = bf16_at(sbase + SM_S1, r0 + j, rl);
+            float mv = f32_at(sbase + SM_S0, r0 + j, rl);
+            if (apply) {
+              mv = fmaf(st.mu, mv, gv);
+              f32_put(sbase + SM_S0, r0 + j, rl, mv);
+            }
+            y[j] = st.nesterov ? fmaf(st.mu, mv, gv) : mv;
+          } else {
+            y[j] = f32_at(sbase + SM_S0, r0 + j, rl);
+          }
+        }
+      } else if (fmt == FMT_G16) {
+        ld_bf16_32(sbase + SM_S1, r, c, y);
+      } else if (fmt == FMT_G16M32) {
+        float mv[32];
+        ld_bf16_32(sbase + SM_S1, r, c, y);
+        ld_f32_32(sbase + SM_S0, r, c, mv);
+        const uint64_t mu2 = pk2(st.mu, st.mu);
+        if (apply) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            uint64_t x = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(y[j], y[j + 1]));
+            upk2(x, mv[j], mv[j + 1]);
+          }
+          st_f32_32(sbase + SM_S0, r, c, mv);
+        }
+        if (st.nesterov) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            uint64_t x = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(y[j], y[j + 1]));
+            upk2(x, y[j], y[j + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] = mv[j];
+        }
+      } else {
+        ld_f32_32(sbase + SM_S0, r, c, y);
+      }
+    };
+
     int64_t g = s;
     for (int64_t base = first_tile + s * stride_tiles; base < tile_end;
          base += 2 * stride_tiles, g += 2) {
-      wait_bar(b_full[s], static_cast<uint32_t>((g >> 1) & 1), wait_ns, abort_flag, err);
+      if (issuer)
+        wait_bar(b_full[s], static_cast<uint32_t>((g >> 1) & 1), wait_ns, abort_flag, err);
+      named_sync(2 + s, SLOT_THREADS);
       const int mi = ctl.info_mi[t];
       const int i0 = ctl.info_i0[t], j0 = ctl.info_j0[t];
       const int th = ctl.info_h[t], tw = ctl.info_w[t];
       const int fmt = ctl.info_fmt[t];
-      const float snorm = ctl.info_s[t];
+      const float s_info = ctl.info_s[t];
 
-      // ---- prologue: staging -> sX = U_bf and R_X = s (a U - e U_bf). The input
-      // itself (exact for bf16 G) is the first step's operand; the normalisation
-      // factor s is applied to the first step's fp32 epilogue values instead, so
-      // that X_0 = s U is never rounded to bf16 a second time.
+      // ---- prologue: staging -> sX = U_bf and R_X = a U - e U_bf, with the sum
+      // of squares of U for the normalisation. The input itself (exact for bf16
+      // G) is the first step's operand; the normalisation factor s enters the
+      // first step's fp32 epilogue values instead (A = s^2 U_bf U_bf^T, and the
+      // third product yields X_1 / s), so that X_0 = s U is never rounded twice.
       // A wide tile (fewer valid rows than columns) runs transposed: X^T has the
       // same map (p(X)^T = p(X^T)), and with the short side as the Gram's side
       // the bf16 rounding of X enters B X through a projection that averages
       // it over the long side, instead of elementwise.
       const bool tr = th < tw;
+      if (STEP && mi >= 0 && !tr && rl < th && cbase < tw) {
+        // the weights this thread updates at the end of the tile: pull them into
+        // L2 now, so that the final update does not wait on DRAM
+        const MatDesc& d = descs[mi];
+        const bool out32 = d.flags & F_OUT_FP32;
+        const char* wp = gptr(d.out, d.ld_out, i0 + rl, j0 + cbase, out32);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(wp));
+        if (out32 && HALF * 4 > 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(wp + 128));
+      }
+      float ssq = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < NCH; ++ch) {
         const int c = cbase + 32 * ch;
         float y[32];
-        if (tr) {
-          const int r0 = t * T + c;          // stage row of tile row c
+        read_u(fmt, tr, c, true, y);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (fmt == FMT_G16) {
-              y[j] = bf16_at(sbase + SM_S1, r0 + j, rl);
-            } else if (fmt == FMT_G16M32) {
-              const float mv = f32_at(sbase + SM_S0, r0 + j, rl);
-              y[j] = st.nesterov ? fmaf(st.mu, mv, bf16_at(sbase + SM_S1, r0 + j, rl)) : mv;
-            } else {
-              y[j] = f32_at(sbase + SM_S0, r0 + j, rl);
-            }
-          }
-        } else if (fmt == FMT_G16) {
-          ld_bf16_32(sbase + SM_S1, r, c, y);
-        } else if (fmt == FMT_G16M32) {
-          float mv[32];
-          ld_bf16_32(sbase + SM_S1, r, c, y);
-          ld_f32_32(sbase + SM_S0, r, c, mv);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) y[j] = st.nesterov ? fmaf(st.mu, mv[j], y[j]) : mv[j];
-        } else {
-          ld_f32_32(sbase + SM_S0, r, c, y);
-        }
-        if (K == 0) {
-          scale32(y, snorm);
-          if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, y);
-          continue;
-        }
+        for (int j = 0; j < 32; ++j) ssq = fmaf(y[j], y[j], ssq);
+        if (K == 0) continue;
         uint32_t pkd[16];
         st_bf16_32(sx, r, c, y, pkd);
-        const uint64_t a2 = pk2(snorm * ns.a, snorm * ns.a), ne2 = pk2(-snorm * e, -snorm * e);
+        const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           uint64_t x = fma2(a2, pk2(y[2 * j], y[2 * j + 1]),
@@ -711,19 +760,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         ptx::tmem_st32(t_x + c, y);
       }
-      // staging consumed
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_empty);
-      if (K == 0) continue;
-      hand_over(true, true, 0);            // -> X X^T
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+      if (lane == 0) ctl.part[s][ws] = ssq;
+
+      // normalisation factor of this thread's tile (partials summed in a fixed order)
+      auto tile_scale = [&]() -> float {
+        if (ns.norm != NORM_TILE) return s_info;
+        float acc = 0.f;
+        if (T == 128) {
+#pragma unroll
+          for (int w = 0; w < 8; ++w) acc += ctl.part[s][w];
+        } else {
+          acc = ((ctl.part[s][2 * t] + ctl.part[s][2 * t + 1]) + ctl.part[s][2 * t + 4]) +
+                ctl.part[s][2 * t + 5];
+        }
+        return 1.f / (sqrtf(acc) + ns.eps);
+      };
+
+      if (K == 0) {
+        // no iteration: the output is s U, which needs the whole tile's sum of
+        // squares first, so U is read a second time (momentum already applied)
+        ptx::fence_proxy_async_smem();
+        named_sync(2 + s, SLOT_THREADS);
+        const float sc_t = tile_scale();
+#pragma unroll 1
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int c = cbase + 32 * ch;
+          float y[32];
+          read_u(fmt, tr, c, false, y);
+          scale32(y, sc_t);
+          if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, y);
+        }
+        named_sync(2 + s, SLOT_THREADS);
+        if (issuer) mbar_arrive(b_empty);
+        continue;
+      }
+      ptx::tmem_wait_st();
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      named_sync(2 + s, SLOT_THREADS);
+      if (issuer) mbar_arrive(b_empty);    // staging read: the loader may refill it
+      issue(0);                            // -> X X^T
+      const float sc_t = tile_scale();
+      const float s2 = sc_t * sc_t;
 
 #pragma unroll 1
-      const float s2 = snorm * snorm;
       for (int k = 0; k < K; ++k) {
         // ---- E1: A = X X^T in R_A
-        wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
-        acc_ph ^= 1u;
-        ptx::tc_fence_after();
+        wait_acc();
 #pragma unroll 1
         for (int ch = 0; ch < NCH; ++ch) {
           const int c = cbase + 32 * ch;
@@ -733,61 +818,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (has_c) {
             if (k == 0) scale32(v, s2);              // A = s^2 U_bf U_bf^T
             st_bf16_32(sc, r, c, v, pkd);            // A_bf
-            // pre-init (b/c) A_bf + (e/c) I: the b A term takes the same rounded
-            // A as the A A product, so B is evaluated exactly at A_bf and the
-            // rounding enters through dB/dA = b + 2 c A, which is small where
-            // the two terms nearly cancel, instead of through 2 c A alone.
-            const uint64_t bc2 = pk2(bc, bc);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              uint64_t x = mul2(bc2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j])));
-              upk2(x, v[2 * j], v[2 * j + 1]);
-            }
-            if ((rl >> 5) == (c >> 5)) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? ec : 0.f;
-            }
-            ptx::tmem_st32(t_a + c, v);
           } else {
-            // C = b A + e I; on the first step s C, as the operand there is U_bf
-            scale32(v, k == 0 ? ns.b * s2 * snorm : ns.b);
-            const float dg = k == 0 ? e * snorm : e;
+            scale32(v, k == 0 ? ns.b * s2 : ns.b);   // C = b A + e I
             if ((rl >> 5) == (c >> 5)) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? dg : 0.f;
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
             }
             st_bf16_32(sc, r, c, v, pkd);
           }
         }
-        hand_over(true, has_c, has_c ? 1 : 2);   // -> A A (or C X)
+        hand_over(true, false, has_c ? 1 : 2);   // -> A A (or C X)
 
         if (has_c) {
-          // ---- E2: R_A = (b/c) A + A A + (e/c) I  ->  C = c R_A
-          wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
-          acc_ph ^= 1u;
-          ptx::tc_fence_after();
+          // ---- E2: R_A = A_bf A_bf  ->  C = c A_bf A_bf + b A_bf + e I. The b A
+          // term takes the same rounded A_bf as the product (read back from sC),
+          // so B is evaluated exactly at A_bf and its rounding enters through
+          // dB/dA = b + 2 c A, small where the two terms nearly cancel, instead
+          // of through 2 c A alone.
+          wait_acc();
 #pragma unroll 1
           for (int ch = 0; ch < NCH; ++ch) {
             const int c = cbase + 32 * ch;
-            float v[32];
+            float v[32], av[32];
             ptx::tmem_ld32_sync(t_a + c, v);
-            scale32(v, k == 0 ? ns.c * snorm : ns.c);   // first step: s C (operand U_bf)
+            ld_bf16_32(sc, r, c, av);
+            const uint64_t c2 = pk2(ns.c, ns.c), b2 = pk2(ns.b, ns.b);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              uint64_t x = fma2(c2, pk2(v[j], v[j + 1]), mul2(b2, pk2(av[j], av[j + 1])));
+              upk2(x, v[j], v[j + 1]);
+            }
+            if ((rl >> 5) == (c >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
+            }
             uint32_t pkd[16];
             st_bf16_32(sc, r, c, v, pkd);
           }
           hand_over(true, false, 2);       // -> C X
         }
 
-        // ---- E3: R_X = X'
-        wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
-        acc_ph ^= 1u;
-        ptx::tc_fence_after();
+        // ---- E3: R_X = X' (on the first step X_1 / s)
+        wait_acc();
         const bool last = (k + 1 == K);
 #pragma unroll 1
         for (int ch = 0; ch < NCH; ++ch) {
           const int c = cbase + 32 * ch;
           float v[32];
           ptx::tmem_ld32_sync(t_x + c, v);
+          if (k == 0) scale32(v, sc_t);
           if (last) {
             if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, v);
           } else {
