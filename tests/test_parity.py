@@ -232,6 +232,65 @@ def test_step_weight_decay_and_fp32_weights():
     assert np.linalg.norm(d_gpu - d_ref) <= TOL_BF16 * np.linalg.norm(d_ref)
 
 
+# ---------------------------------------------------------------- large tiles and full matrix (GEMM path)
+
+@pytest.mark.parametrize("H,W,T", [(300, 530, 256), (1000, 300, 256), (513, 200, 384),
+                                   (600, 640, 4096), (1024, 1024, 1024), (130, 700, 96)])
+def test_gemm_path_matches_oracle(H, W, T):
+    G = synth.lowrank_noise(H, W, seed=H + 3 * W + T)
+    out = hm.tiled_ns(G.cuda(), T, 5, path="tensor", out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+
+
+def test_full_matrix_equals_one_tile_and_differs_from_tiled():
+    G = synth.lowrank_noise(512, 768, seed=77).cuda()
+    full = hm.tiled_ns(G, 768, 5, path="tensor", out_dtype=torch.float32)
+    full2 = hm.tiled_ns(G, 4096, 5, path="tensor", out_dtype=torch.float32)
+    assert torch.equal(full, full2)                       # any T >= max(H, W): one tile
+    want = oracle.full_ns(f64(G), 5)
+    assert rel_fro(f64(full), want) <= TOL_BF16
+    tiled = hm.tiled_ns(G, 128, 5, out_dtype=torch.float32)
+    assert rel_fro(f64(tiled), want) > 0.05               # a local map, not the full one
+
+
+def test_gemm_path_4096_t256_sampled_tiles():
+    # 4096 x 4096 at T = 256: 256 independent tiles; the oracle checks a sample
+    G = synth.lowrank_noise(4096, 4096, seed=5, device="cuda")
+    out = hm.tiled_ns(G, 256, 5, path="tensor", out_dtype=torch.float32)
+    rng = np.random.default_rng(0)
+    for ti, tj in rng.integers(0, 16, size=(6, 2)):
+        sl = (slice(256 * ti, 256 * ti + 256), slice(256 * tj, 256 * tj + 256))
+        want = oracle.tiled_ns(f64(G[sl]), 256, 5)
+        assert rel_fro(f64(out[sl]), want) <= TOL_BF16
+
+
+def test_gemm_path_step_matches_oracle():
+    shapes = [(768, 768), (300, 530), (1000, 300)]
+    Ws, Gs, Ms = _step_case(shapes, 90)
+    W0 = [f64(w) for w in Ws]
+    M0 = [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, 256, 5, lr=0.02, mu=0.95, nesterov=True, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 256, 5, lr=0.02, mu=0.95)
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        d_gpu, d_ref = f64(Ws[i]) - W0[i], Wn - W0[i]
+        bound = TOL_BF16 * np.linalg.norm(d_ref) + np.linalg.norm(np.abs(Wn) * 2.0 ** -8)
+        assert np.linalg.norm(d_gpu - d_ref) <= bound
+
+
+def test_gemm_path_chunking_and_batching_bit_exact():
+    shapes = [(600, 520), (300, 1030), (257, 257)]
+    Gs = [synth.lowrank_noise(H, W, seed=40 + i).cuda() for i, (H, W) in enumerate(shapes)]
+    ref = hm.tiled_ns_batched(Gs, 256, 5, path="tensor")
+    for chunk in (1, 256 * 256 * 2 * 3 + 5):
+        outs = hm.tiled_ns_batched(Gs, 256, 5, path="tensor", chunk_bytes=chunk)
+        for a, b in zip(ref, outs):
+            assert torch.equal(a, b)
+    for G, O in zip(Gs, ref):
+        assert torch.equal(hm.tiled_ns(G, 256, 5, path="tensor"), O)
+
+
 # ---------------------------------------------------------------- errors
 
 def test_bad_arguments_raise_without_launch():
@@ -244,7 +303,7 @@ def test_bad_arguments_raise_without_launch():
     with pytest.raises(hm.HimuonError):
         hm.tiled_ns(G, 128, 5, out=G[:, :3])
     with pytest.raises(hm.HimuonError) as e:
-        hm.tiled_ns(G, 96, 5, path="tensor")         # no tensor kernel for T = 96
+        hm.tiled_ns(G, 32, 5, path="tensor")         # no tensor kernel for T = 32
     assert e.value.status_name == "UNSUPPORTED"
     big = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(hm.HimuonError):               # partial overlap of out and G

@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <string>
 #include <vector>
 
@@ -97,6 +98,8 @@ struct himuon_handle {
   float* scratch = nullptr;    // fp32-path tile buffers
   size_t scratch_bytes = 0;
   int* d_err = nullptr;        // device error word
+  void* tiles = nullptr;       // GEMM-path tile table
+  size_t tiles_bytes = 0;
   uint64_t wait_ns = 2000000000ull;
   int64_t launches = 0;        // kernels launched through this handle
   std::vector<unsigned char> host;
@@ -161,6 +164,28 @@ bool make_map(CUtensorMap* m, const void* base, int64_t H, int64_t W, int64_t ld
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+namespace himuon {
+bool encode_map_3d(void* map, const void* base, int64_t C, int64_t R, int64_t n, int box_c,
+                   int box_r) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R),
+                        static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(C * 2), static_cast<cuuint64_t>(C * R * 2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_c), static_cast<cuuint32_t>(box_r), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+}  // namespace himuon
+
+namespace {
+
 himuon_status check_handle(himuon_handle* h) {
   if (!h) return fail(HIMUON_ERR_INVALID_ARG, "handle is NULL");
   int dev = -1;
@@ -168,6 +193,70 @@ himuon_status check_handle(himuon_handle* h) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev != h->device)
     return fail(HIMUON_ERR_INVALID_ARG, "handle was created on another device than the current one");
+  return HIMUON_OK;
+}
+
+constexpr int64_t kGemmScratchCap = int64_t(2) << 30;  // scratch bytes of one GEMM-path batch
+
+// Large tiles and the full-matrix map: every tile becomes a chain of GEMMs.
+// Tiles are oriented so that the Gram matrix is on the short side, padded to
+// multiples of 128, grouped by padded shape and run in batches whose scratch
+// stays within kGemmScratchCap.
+himuon_status run_gemm_path(himuon_handle* h, const std::vector<MatDesc>& descs,
+                            const MatDesc* d_descs, int32_t T, const NSArgs& ns,
+                            const StepArgs& st,
+                            const std::vector<std::pair<int64_t, int64_t>>& chunks,
+                            cudaStream_t stream) {
+  auto r128 = [](int64_t x) { return static_cast<int>((x + 127) / 128 * 128); };
+  for (const auto& c : chunks) {
+    // tiles of this chunk, grouped by padded oriented shape
+    std::map<std::pair<int, int>, std::vector<GTile>> groups;
+    for (size_t mi = 0; mi < descs.size(); ++mi) {
+      const MatDesc& d = descs[mi];
+      const int64_t lo = std::max<int64_t>(c.first, d.tile_start);
+      const int64_t hi = std::min<int64_t>(c.second, d.tile_start + d.ntiles);
+      for (int64_t t = lo; t < hi; ++t) {
+        const int64_t lt = t - d.tile_start;
+        GTile g{};
+        g.mi = static_cast<int32_t>(mi);
+        g.i0 = static_cast<int32_t>(lt / d.tiles_w) * T;
+        g.j0 = static_cast<int32_t>(lt % d.tiles_w) * T;
+        g.h = std::min<int32_t>(T, d.H - g.i0);
+        g.w = std::min<int32_t>(T, d.W - g.j0);
+        g.tr = g.h > g.w ? 1 : 0;
+        g.s = 1.f;
+        groups[{r128(std::min(g.h, g.w)), r128(std::max(g.h, g.w))}].push_back(g);
+      }
+    }
+    for (auto& kv : groups) {
+      const int Hp = kv.first.first, Wp = kv.first.second;
+      const int64_t per = gemm_scratch_bytes(Hp, Wp);
+      const int64_t nb = std::max<int64_t>(1, std::min<int64_t>(kGemmScratchCap / per, 1 << 20));
+      const std::vector<GTile>& all = kv.second;
+      for (size_t b0 = 0; b0 < all.size(); b0 += static_cast<size_t>(nb)) {
+        const int nt = static_cast<int>(std::min<size_t>(static_cast<size_t>(nb), all.size() - b0));
+        void* scr = h->scratch;
+        himuon_status s = grow(&scr, &h->scratch_bytes, static_cast<size_t>(per * nt), stream,
+                               "GEMM-path scratch");
+        h->scratch = static_cast<float*>(scr);
+        if (s != HIMUON_OK) return s;
+        void* tl = h->tiles;
+        s = grow(&tl, &h->tiles_bytes, sizeof(GTile) * nt, stream, "tile table");
+        h->tiles = tl;
+        if (s != HIMUON_OK) return s;
+        // pageable source: staged before the call returns
+        cudaError_t e = cudaMemcpyAsync(h->tiles, all.data() + b0, sizeof(GTile) * nt,
+                                        cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tile table upload");
+        himuon_status ms = HIMUON_OK;
+        e = launch_ns_gemm_batch(static_cast<const GTile*>(h->tiles), nt, Hp, Wp, d_descs, ns, st,
+                                 h->scratch, h->wait_ns, h->d_err, stream, &ms);
+        if (ms != HIMUON_OK) return fail(ms, "GEMM path: tensor map encoding failed");
+        if (e != cudaSuccess) return cuda_fail(e, "GEMM path launch");
+        h->launches += 2 + (ns.K == 0 ? 1 : ns.K * (ns.c != 0.f ? 3 : 2));
+      }
+    }
+  }
   return HIMUON_OK;
 }
 
@@ -197,18 +286,19 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   }
 
   const bool fp32 = p.path == HIMUON_PATH_FP32;
-  const bool full = T >= maxside;  // one tile per matrix: the full-matrix map
-  if (!fp32 && T != 128 && T != 64) {
+  // tensor path: T = 64 and 128 run on chip (ns_tc.cu); T > 64 otherwise, and
+  // the full-matrix map, run as batched GEMMs (ns_gemm.cu)
+  const bool onchip = T == 64 || T == 128;
+  if (!fp32 && !onchip && T < 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
-                    (full ? " (full-matrix)" : "") + " is not implemented in this build; "
-                    "use T = 64 or 128, or the fp32 path");
+                    " is not implemented in this build; use T >= 64, or the fp32 path");
   }
 
   // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
   // step bf16 G and fp32 M); other matrices are staged with plain loads.
-  std::vector<CUtensorMap> maps(fp32 ? 0 : 2 * static_cast<size_t>(n));
-  for (int i = 0; i < n && !fp32; ++i) {
+  std::vector<CUtensorMap> maps((fp32 || !onchip) ? 0 : 2 * static_cast<size_t>(n));
+  for (int i = 0; i < n && !fp32 && onchip; ++i) {
     MatDesc& d = descs[i];
     const bool in32 = d.flags & F_IN_FP32;
     bool ok = (d.flags & F_IN_VEC) != 0;
@@ -304,13 +394,16 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
     return HIMUON_OK;
   }
 
-  for (auto& c : chunks) {
-    e = launch_ns_tc(d_descs, d_maps, n, c.first, c.second, ns, st, h->wait_ns, h->d_err,
-                     h->num_sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
-    h->launches += 1;
+  if (onchip) {
+    for (auto& c : chunks) {
+      e = launch_ns_tc(d_descs, d_maps, n, c.first, c.second, ns, st, h->wait_ns, h->d_err,
+                       h->num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
+      h->launches += 1;
+    }
+    return HIMUON_OK;
   }
-  return HIMUON_OK;
+  return run_gemm_path(h, descs, d_descs, T, ns, st, chunks, stream);
 }
 
 // Under HIMUON_PATH_AUTO, matrices this small or thin run on the fp32 path:
@@ -418,6 +511,7 @@ himuon_status himuon_destroy(himuon_handle* h) {
   cudaDeviceSynchronize();
   if (h->ws) cudaFree(h->ws);
   if (h->scratch) cudaFree(h->scratch);
+  if (h->tiles) cudaFree(h->tiles);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
   return HIMUON_OK;

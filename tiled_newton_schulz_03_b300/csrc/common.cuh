@@ -42,6 +42,16 @@ static_assert(sizeof(MatDesc) == 96, "MatDesc layout");
 
 enum : int32_t { NORM_TILE = 0, NORM_MATRIX = 1, NORM_NONE = 2 };
 
+// One tile of the batched-GEMM path (large T): matrix, origin, valid extent,
+// whether it is processed transposed (more rows than columns), and its
+// normalisation factor (written on the device).
+struct GTile {
+  int32_t mi, i0, j0, h, w, tr;
+  float s;
+  float pad_;
+};
+static_assert(sizeof(GTile) == 32, "GTile layout");
+
 struct NSArgs {
   float a, b, c, eps;
   int32_t norm;

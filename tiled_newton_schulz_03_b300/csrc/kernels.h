@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <string>
 
+#include "../../include/himuon.h"
 #include "common.cuh"
 
 namespace himuon {
@@ -38,6 +39,21 @@ constexpr int NORM_ROWS_PER_PART = 32;
 // One CTA waits on an mbarrier that nothing arrives on, for wait_ns, then
 // records a time-out in *err and returns (aux_kernels.cu).
 cudaError_t launch_wait_selftest(uint64_t wait_ns, int* err, cudaStream_t stream);
+
+// Batched-GEMM path for large tiles and the full-matrix map (ns_gemm.cu): n
+// tiles of one padded oriented shape Hp x Wp (multiples of 128, Hp <= Wp),
+// d_tiles their device descriptors, scratch of gemm_scratch_bytes(Hp, Wp) * n
+// bytes. *status is set to a non-OK value if a tensor map cannot be encoded.
+cudaError_t launch_ns_gemm_batch(const GTile* d_tiles, int n, int Hp, int Wp, const MatDesc* descs,
+                                 const NSArgs& ns, const StepArgs& st, void* scratch,
+                                 uint64_t wait_ns, int* err, cudaStream_t stream,
+                                 himuon_status* status);
+int64_t gemm_scratch_bytes(int Hp, int Wp);
+
+// 3-D tiled bf16 tensor map over n row-major C x R matrices stored back to back,
+// box of box_c columns x box_r rows x 1, 128-byte swizzle, zero fill (api.cu).
+bool encode_map_3d(void* map, const void* base, int64_t C, int64_t R, int64_t n, int box_c,
+                   int box_r);
 
 // Sets the message himuon_last_error_string() returns on this host thread (api.cu).
 void record_last_error(const std::string& msg);
