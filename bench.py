@@ -406,19 +406,111 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- secondary workloads
+
+def _timed(fn, reps, flush, stream):
+    """Median CUDA-event time (ms) of fn over reps runs, L2 flushed before each."""
+    import torch
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    return statistics.median(times)
+
+
+def run_sweep(args):
+    """Tile-size sweep on one 4096 x 4096 bf16 matrix (rank-8 + noise), K = 5:
+    tiled NS only, one JSON line per T (T = 4096 is the full-matrix map). The
+    matrix fits in L2, so L2 is flushed (a 256 MB write) before every run."""
+    import torch
+
+    import tiled_newton_schulz_03_b300 as hm
+    from tiled_newton_schulz_03_b300 import build as hbuild, synth
+    hbuild.build()
+    dev = torch.device("cuda", 0)
+    handle = hm.Handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    G = synth.lowrank_noise(4096, 4096, seed=3, rank=8, device=dev)
+    out = torch.empty_like(G)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    peaks, src = load_peaks()
+    for T in (32, 64, 128, 256, 4096):
+        fn = lambda: hm.tiled_ns(G, T, 5, out=out, handle=handle, stream=stream)
+        for _ in range(args.warmup):
+            fn()
+        ms = _timed(fn, args.steps, flush, stream)
+        flops = 6.0 * 4096 * 4096 * min(T, 4096) * 5
+        tf = flops / (ms * 1e-3) / 1e12
+        hbm_ms = 4.0 * 4096 * 4096 / (float(peaks.get("hbm_gbs", 6400.0)) * 1e9) * 1e3
+        print(json.dumps({"workload": "sweep4096", "T": T, "K": 5, "ms": round(ms, 4),
+                          "tflops": round(tf, 2), "frac_of_burst_bf16": round(tf / float(peaks.get("bf16_tflops", 1800.0)), 4),
+                          "roofline_ms": round(max(flops / (float(peaks.get("bf16_tflops", 1800.0)) * 1e12) * 1e3, hbm_ms), 4),
+                          "peak_source": src}), flush=True)
+    assert hm.device_error(handle=handle) == 0
+    handle.close()
+
+
+def run_ragged(args):
+    """Ragged shapes and the runtime tile schedule: 1000x3000, 5120x13824 and
+    2048x50257 bf16 (rank-8 + noise), three successive fused steps with T = 64,
+    128, 256, for K = 3 and 5; one JSON line per (K, step)."""
+    import torch
+
+    import tiled_newton_schulz_03_b300 as hm
+    from tiled_newton_schulz_03_b300 import build as hbuild, synth
+    hbuild.build()
+    dev = torch.device("cuda", 0)
+    handle = hm.Handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    shapes = [(1000, 3000), (5120, 13824), (2048, 50257)]
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    sched = hm.TSchedule([(0, 64), (1, 128), (2, 256)])
+    for K in (3, 5):
+        Ws = [synth.gaussian(H, W, seed=10 + i, std=0.02, dtype=torch.bfloat16, device=dev) for i, (H, W) in enumerate(shapes)]
+        Ms = [torch.zeros(H, W, device=dev) for H, W in shapes]
+        for step in range(3):
+            Gs = [synth.lowrank_noise(H, W, seed=100 * step + i, rank=8, device=dev) for i, (H, W) in enumerate(shapes)]
+            T = sched(step)
+            # time copies of the state, so that every timed run does the same step
+            Wc = [w.clone() for w in Ws]
+            Mc = [m.clone() for m in Ms]
+            fn = lambda: hm.step(Wc, Gs, Mc, T, K, lr=0.02, mu=0.95, handle=handle, stream=stream)
+            for _ in range(args.warmup):
+                fn()
+            ms = _timed(fn, args.steps, flush, stream)
+            hm.step(Ws, Gs, Ms, T, K, lr=0.02, mu=0.95, handle=handle, stream=stream)
+            flops = sum(6.0 * H * W * T * K for H, W in shapes)
+            print(json.dumps({"workload": "ragged", "K": K, "step": step, "T": T, "ms": round(ms, 4),
+                              "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}), flush=True)
+    assert hm.device_error(handle=handle) == 0
+    handle.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3_8b")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["sweep4096", "ragged"],
+                    default="llama3_8b",
+                    help="llama3_8b (headline) or gpt2_small: the fused step, one JSON line; "
+                         "sweep4096 / ragged: secondary per-configuration timings")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.workload == "sweep4096" and args.impl == "ours":
+        run_sweep(args)
+    elif args.workload == "ragged" and args.impl == "ours":
+        run_ragged(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -44,6 +44,7 @@ def built():
 # ---------------------------------------------------------------- one matrix
 
 @pytest.mark.parametrize("T,path,tol", [(128, "tensor", TOL_BF16), (64, "tensor", TOL_BF16),
+                                        (32, "tensor", TOL_BF16),
                                         (64, "fp32", TOL_FP32), (128, "fp32", TOL_FP32),
                                         (32, "fp32", TOL_FP32)])
 def test_gaussian_fp32_256x512(T, path, tol):
@@ -56,7 +57,7 @@ def test_gaussian_fp32_256x512(T, path, tol):
 @pytest.mark.parametrize("H,W", [(300, 530), (128, 128), (1, 1), (1, 300), (257, 3),
                                  (129, 255), (768, 3072)])
 @pytest.mark.parametrize("path", ["tensor", "fp32"])
-@pytest.mark.parametrize("T", [128, 64])
+@pytest.mark.parametrize("T", [128, 64, 32])
 def test_lowrank_bf16_ragged(H, W, path, T):
     G = synth.lowrank_noise(H, W, seed=H * 7 + W)
     out = hm.tiled_ns(G.cuda(), T, 5, path=path, out_dtype=torch.float32)
@@ -204,6 +205,23 @@ def test_step_zero_lr_keeps_weights_and_updates_momentum():
     assert rel_fro(f64(Ms[0]), 0.9 * M0 + f64(Gs[0])) <= 1e-6
 
 
+def test_t32_step_and_chunking():
+    shapes = [(300, 200), (96, 500)]
+    Ws, Gs, Ms = _step_case(shapes, 95)
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, 32, 5, lr=0.02, mu=0.95, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 32, 5, lr=0.02, mu=0.95)
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        d_gpu, d_ref = f64(Ws[i]) - W0[i], Wn - W0[i]
+        bound = TOL_BF16 * np.linalg.norm(d_ref) + np.linalg.norm(np.abs(Wn) * 2.0 ** -8)
+        assert np.linalg.norm(d_gpu - d_ref) <= bound
+    ref = hm.tiled_ns_batched(Gs, 32, 5, path="tensor")
+    outs = hm.tiled_ns_batched(Gs, 32, 5, path="tensor", chunk_bytes=3 * 32 * 32 * 2 + 1)
+    for a, b in zip(ref, outs):
+        assert torch.equal(a, b)
+
+
 def test_step_three_successive_steps_with_tile_schedule():
     shapes = [(1000, 3000 // 4), (2048, 503)]
     Ws, _, Ms = _step_case(shapes, 70)
@@ -303,7 +321,7 @@ def test_bad_arguments_raise_without_launch():
     with pytest.raises(hm.HimuonError):
         hm.tiled_ns(G, 128, 5, out=G[:, :3])
     with pytest.raises(hm.HimuonError) as e:
-        hm.tiled_ns(G, 32, 5, path="tensor")         # no tensor kernel for T = 32
+        hm.tiled_ns(G, 16, 5, path="tensor")         # no tensor kernel for T = 16
     assert e.value.status_name == "UNSUPPORTED"
     big = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(hm.HimuonError):               # partial overlap of out and G

@@ -288,20 +288,21 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   const bool fp32 = p.path == HIMUON_PATH_FP32;
   // tensor path: T = 64 and 128 run on chip (ns_tc.cu); T > 64 otherwise, and
   // the full-matrix map, run as batched GEMMs (ns_gemm.cu)
-  const bool onchip = T == 64 || T == 128;
+  const bool onchip = T == 32 || T == 64 || T == 128;
   if (!fp32 && !onchip && T < 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
-                    " is not implemented in this build; use T >= 64, or the fp32 path");
+                    " is not implemented in this build; use T = 32 or T >= 64, or the fp32 path");
   }
 
   // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
-  // step bf16 G and fp32 M); other matrices are staged with plain loads.
+  // step bf16 G and fp32 M; T >= 64, since a 32-column box is narrower than the
+  // 128-byte staging rows); other matrices are staged with plain loads.
   std::vector<CUtensorMap> maps((fp32 || !onchip) ? 0 : 2 * static_cast<size_t>(n));
   for (int i = 0; i < n && !fp32 && onchip; ++i) {
     MatDesc& d = descs[i];
     const bool in32 = d.flags & F_IN_FP32;
-    bool ok = (d.flags & F_IN_VEC) != 0;
+    bool ok = (d.flags & F_IN_VEC) != 0 && T >= 64;
     if (st.enabled) ok = ok && !in32 && (d.flags & F_M_VEC) && !(d.flags & F_M_BF16);
     std::memset(&maps[2 * i], 0, 2 * sizeof(CUtensorMap));
     if (ok) ok = make_map(&maps[2 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
