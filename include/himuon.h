@@ -123,9 +123,10 @@ void himuon_default_ns_params(himuon_ns_params* p);
  * Tiled NS map of one matrix (abstract, sentences 3-5).
  * G: H x W input, ld ldg, dtype gtype (BF16 or FP32).
  * out: H x W output, ld ldo, dtype otype (BF16 or FP32); may be G itself.
- * T: tile size, 1 <= T; the tensor path implements T in {32, 64, 128, 256} and
- *    T >= max(H, W) (one tile = the full-matrix map of Muon, sentences 1-2);
- *    other T return HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any T.
+ * T: tile size, 1 <= T. The tensor path runs T = 32, 64 and 128 on chip and
+ *    every T >= 65 (including 256, and T >= max(H, W): one tile = the
+ *    full-matrix map of Muon, sentences 1-2) as batched GEMMs; other T (below 64,
+ *    except 32) return HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any T.
  * K: number of NS steps, 0 <= K <= 64.
  * params: NULL means the defaults.
  * Returns HIMUON_ERR_INVALID_ARG for H or W < 1, ld < W, NULL pointers, bad
