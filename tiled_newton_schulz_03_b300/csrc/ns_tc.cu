@@ -648,12 +648,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       issue(p);
     };
 
-    // Waits for the slot's last product: one thread polls, the slot syncs
-    // (warps waiting at a barrier take no issue slots from the working ones).
+    // Waits for the slot's last product.
     auto wait_acc = [&]() {
-      if (issuer) wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
+      // every thread waits itself (sleeping in try_wait, no issue slots taken):
+      // no barrier hop between the poller and the others
+      wait_bar(b_acc[s], acc_ph, wait_ns, abort_flag, err);
       acc_ph ^= 1u;
-      named_sync(2 + s, SLOT_THREADS);
       ptx::tc_fence_after();
     };
 
@@ -865,6 +865,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ch = 0; ch < nch; ++ch) {
           const int c = cbase + 32 * ch;
           float v[32];
+          ptx::tmem_ld32_sync(t_x + c, v);
+            if (k == 0) scale32(v, sc_t);
+            const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale);
+            const uint64_t wdf = pk2(st.wd_factor, st.wd_factor);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              uint64_t x = fma2(nls, pk2(v[j], v[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1])));
+              upk2(x, wv[j], wv[j + 1]);
+            }
+            if (n > 0) gstore32(op, c, n, out32, d.flags & F_OUT_VEC, wv);
+            continue;
+          }
           ptx::tmem_ld32_sync(t_x + c, v);
           if (k == 0) scale32(v, sc_t);
           if (last) {
