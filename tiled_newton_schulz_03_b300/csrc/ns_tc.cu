@@ -866,18 +866,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int c = cbase + 32 * ch;
           float v[32];
           ptx::tmem_ld32_sync(t_x + c, v);
-            if (k == 0) scale32(v, sc_t);
-            const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale);
-            const uint64_t wdf = pk2(st.wd_factor, st.wd_factor);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              uint64_t x = fma2(nls, pk2(v[j], v[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1])));
-              upk2(x, wv[j], wv[j + 1]);
-            }
-            if (n > 0) gstore32(op, c, n, out32, d.flags & F_OUT_VEC, wv);
-            continue;
-          }
-          ptx::tmem_ld32_sync(t_x + c, v);
           if (k == 0) scale32(v, sc_t);
           if (last) {
             if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, v);
