@@ -72,7 +72,7 @@ enum : int { FMT_U32 = 0, FMT_G16 = 1, FMT_G16M32 = 2 };
 
 struct Ctl {
   uint64_t acc_full[2];   // tensor core -> slot: the slot's last product is complete
-  uint64_t st_full[2];    // loader -> slot s: staging holds this slot's next stage
+  uint64_t st_full[2];    // loader -> slots: staging holds stage g (barrier g % 2)
   uint64_t st_empty;      // slot -> loader: staging has been read
   uint64_t st_loaded;     // TMA -> loader: staging bytes have landed
   uint64_t drain[2];      // slot issuer: all its MMAs complete (abort path)
@@ -81,6 +81,8 @@ struct Ctl {
   float part[2][8];       // per slot warp: sum of squares of its row segments
   int info_mi[4], info_i0[4], info_j0[4], info_h[4], info_w[4], info_fmt[4];
   float info_s[4];
+  int ticket;             // next stage to hand to a free slot
+  int ticket_s[2];        // the stage each slot took
 };
 
 // ------------------------------------------------------------------ layouts
@@ -348,6 +350,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::mbar_init(b_loaded, 1);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
+    ctl.ticket = 0;
   }
   if (warp == 0) {
     ptx::tmem_alloc(ptx::smem_u32(&ctl.tmem_base), TMEM_COLS);
@@ -711,11 +714,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     };
 
-    int64_t g = s;
-    for (int64_t base = first_tile + s * stride_tiles; base < tile_end;
-         base += 2 * stride_tiles, g += 2) {
+    // A slot that is free takes the next stage in load order (a ticket from a
+    // shared counter), so whichever slot finishes first is served first. Stage
+    // g is signalled on st_full[g % 2]; the two slots hold consecutive tickets,
+    // so they never wait on the same barrier at different phases.
+    for (;;) {
+      if (issuer) ctl.ticket_s[s] = atomicAdd(&ctl.ticket, 1);
+      named_sync(2 + s, SLOT_THREADS);
+      const int64_t g = ctl.ticket_s[s];
+      const int64_t base = first_tile + g * stride_tiles;
+      if (base >= tile_end) break;
       if (issuer)
-        wait_bar(b_full[s], static_cast<uint32_t>((g >> 1) & 1), wait_ns, abort_flag, err);
+        wait_bar(b_full[g & 1], static_cast<uint32_t>((g >> 1) & 1), wait_ns, abort_flag, err);
       named_sync(2 + s, SLOT_THREADS);
       const int mi = ctl.info_mi[t];
       const int i0 = ctl.info_i0[t], j0 = ctl.info_j0[t];
