@@ -253,7 +253,8 @@ def test_step_weight_decay_and_fp32_weights():
 # ---------------------------------------------------------------- large tiles and full matrix (GEMM path)
 
 @pytest.mark.parametrize("H,W,T", [(300, 530, 256), (1000, 300, 256), (513, 200, 384),
-                                   (600, 640, 4096), (1024, 1024, 1024), (130, 700, 96)])
+                                   (600, 640, 4096), (1024, 1024, 1024), (130, 700, 96),
+                                   (300, 410, 100)])
 def test_gemm_path_matches_oracle(H, W, T):
     G = synth.lowrank_noise(H, W, seed=H + 3 * W + T)
     out = hm.tiled_ns(G.cuda(), T, 5, path="tensor", out_dtype=torch.float32)
@@ -283,14 +284,15 @@ def test_gemm_path_4096_t256_sampled_tiles():
         assert rel_fro(f64(out[sl]), want) <= TOL_BF16
 
 
-def test_gemm_path_step_matches_oracle():
+@pytest.mark.parametrize("T", [256, 100])
+def test_gemm_path_step_matches_oracle(T):
     shapes = [(768, 768), (300, 530), (1000, 300)]
     Ws, Gs, Ms = _step_case(shapes, 90)
     W0 = [f64(w) for w in Ws]
     M0 = [f64(m) for m in Ms]
-    hm.step(Ws, Gs, Ms, 256, 5, lr=0.02, mu=0.95, nesterov=True, path="tensor")
+    hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95, nesterov=True, path="tensor")
     for i in range(len(shapes)):
-        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 256, 5, lr=0.02, mu=0.95)
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], T, 5, lr=0.02, mu=0.95)
         assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
         d_gpu, d_ref = f64(Ws[i]) - W0[i], Wn - W0[i]
         bound = TOL_BF16 * np.linalg.norm(d_ref) + np.linalg.norm(np.abs(Wn) * 2.0 ** -8)

@@ -22,7 +22,8 @@
 // [tile][row][col] so that one 3-D TMA map covers an operand of every tile.
 //
 // GEMM kernel: one 128 x BN output block per CTA (BN = 256, or 128 when the
-// width is not a multiple of 256), K in blocks of 64 through a 4-stage TMA ring;
+// width is not a multiple of 256 or K <= 512), K in blocks of 64 through a
+// 3- or 4-stage TMA ring;
 // warp 0 loads, warp 1 issues tcgen05.mma (M = 128, N = BN, K = 16), warps 2-5
 // read the fp32 accumulator from TMEM (one row per thread) and run the epilogue.
 #include <cuda.h>
@@ -40,7 +41,6 @@
 namespace himuon {
 namespace {
 
-constexpr int STAGES = 4;
 constexpr int GEMM_THREADS = 192;
 constexpr uint32_t A_BYTES = 128 * 64 * 2;
 
@@ -121,8 +121,11 @@ __device__ __forceinline__ void emit_elem(const GTile& t, const MatDesc& d, cons
   else out_store(d, row, col, o);
 }
 
-template <int BN, int MODE, bool BMN>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// STAGES-deep ring; small problems (K <= 512) use 128 x 128 blocks and three
+// stages, so that two CTAs share an SM and one's epilogue overlaps the other's
+// main loop.
+template <int BN, int MODE, bool BMN, int STAGES, int MINB>
+__global__ void __launch_bounds__(GEMM_THREADS, MINB)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                    GemmArgs g) {
   constexpr uint32_t B_BYTES = BN * 64 * 2;
@@ -295,8 +298,55 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                                 ptx::pack_bf16x2(o[8 * qd + 6], o[8 * qd + 7]));
         } else {
           const MatDesc& d = g.descs[t.mi];
+          const int vec_mult = (d.flags & F_OUT_FP32) ? 4 : 8;   // elements per 16 bytes
+          if (!t.tr && r < t.h && c0 + 32 <= t.w && (d.flags & F_OUT_VEC) &&
+              (t.j0 + c0) % vec_mult == 0) {
+            // a whole 32-column row segment: 16-byte accesses
+            const bool out32 = d.flags & F_OUT_FP32;
+            char* rowp = static_cast<char*>(d.out) +
+                         (static_cast<int64_t>(t.i0 + r) * d.ld_out + t.j0 + c0) * (out32 ? 4 : 2);
+            if (g.st.enabled) {
+              float wv[32];
+              if (out32) {
+                const float4* p4 = reinterpret_cast<const float4*>(rowp);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) emit_elem(t, d, g.st, r, c0 + j, o[j]);
+                for (int qd = 0; qd < 8; ++qd) {
+                  const float4 f = p4[qd];
+                  wv[4 * qd] = f.x; wv[4 * qd + 1] = f.y; wv[4 * qd + 2] = f.z; wv[4 * qd + 3] = f.w;
+                }
+              } else {
+                const uint4* p4 = reinterpret_cast<const uint4*>(rowp);
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                  const uint4 u = p4[qd];
+                  const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    wv[8 * qd + 2 * j] = ptx::bf16lo(uw[j]);
+                    wv[8 * qd + 2 * j + 1] = ptx::bf16hi(uw[j]);
+                  }
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = fmaf(-d.upd_scale, o[j], wv[j] * g.st.wd_factor);
+            }
+            if (out32) {
+              float4* p4 = reinterpret_cast<float4*>(rowp);
+#pragma unroll
+              for (int qd = 0; qd < 8; ++qd) p4[qd] = make_float4(o[4 * qd], o[4 * qd + 1], o[4 * qd + 2], o[4 * qd + 3]);
+            } else {
+              uint4* p4 = reinterpret_cast<uint4*>(rowp);
+#pragma unroll
+              for (int qd = 0; qd < 4; ++qd)
+                p4[qd] = make_uint4(ptx::pack_bf16x2(o[8 * qd], o[8 * qd + 1]),
+                                    ptx::pack_bf16x2(o[8 * qd + 2], o[8 * qd + 3]),
+                                    ptx::pack_bf16x2(o[8 * qd + 4], o[8 * qd + 5]),
+                                    ptx::pack_bf16x2(o[8 * qd + 6], o[8 * qd + 7]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) emit_elem(t, d, g.st, r, c0 + j, o[j]);
+          }
         }
       }
     }
@@ -382,23 +432,25 @@ __global__ void ns_gemm_emit0(const GTile* __restrict__ tiles, const MatDesc* __
   for (int c = threadIdx.x & 31; c < Wp; c += 32) emit_elem(t, d, st, r, c, t.s * x32[base + c]);
 }
 
-template <int BN, int MODE, bool BMN>
+template <int BN, int MODE, bool BMN, int STAGES, int MINB>
 cudaError_t launch_gemm(const CUtensorMap& mA, const CUtensorMap& mB, const GemmArgs& g, int n,
                         cudaStream_t stream) {
   const uint32_t smem = STAGES * (A_BYTES + BN * 64 * 2) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<BN, MODE, BMN>,
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<BN, MODE, BMN, STAGES, MINB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t ctas = static_cast<int64_t>(n) * (g.M / 128) * (g.N / BN);
-  ns_gemm_kernel<BN, MODE, BMN><<<static_cast<unsigned>(ctas), GEMM_THREADS, smem, stream>>>(mA, mB, g);
+  ns_gemm_kernel<BN, MODE, BMN, STAGES, MINB>
+      <<<static_cast<unsigned>(ctas), GEMM_THREADS, smem, stream>>>(mA, mB, g);
   return cudaGetLastError();
 }
 
 template <int MODE, bool BMN>
 cudaError_t launch_gemm_bn(const CUtensorMap& mA, const CUtensorMap& mB128, const CUtensorMap& mB256,
                            const GemmArgs& g, int n, cudaStream_t stream) {
-  if (g.N % 256 == 0) return launch_gemm<256, MODE, BMN>(mA, mB256, g, n, stream);
-  return launch_gemm<128, MODE, BMN>(mA, mB128, g, n, stream);
+  if (g.K <= 512) return launch_gemm<128, MODE, BMN, 3, 2>(mA, mB128, g, n, stream);
+  if (g.N % 256 == 0) return launch_gemm<256, MODE, BMN, 4, 1>(mA, mB256, g, n, stream);
+  return launch_gemm<128, MODE, BMN, 4, 1>(mA, mB128, g, n, stream);
 }
 
 }  // namespace
