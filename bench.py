@@ -161,14 +161,23 @@ def ncu_traffic(kernel_src_hash: str):
     return None
 
 
+# The files the timed kernel and its launch plan are built from: a change to
+# any of them makes the committed DRAM counters stale; a change elsewhere (the
+# GEMM path, the fp32 path) does not.
+KERNEL_SOURCES = ("tiled_newton_schulz_03_b300/csrc/api.cu",
+                  "tiled_newton_schulz_03_b300/csrc/common.cuh",
+                  "tiled_newton_schulz_03_b300/csrc/kernels.h",
+                  "tiled_newton_schulz_03_b300/csrc/ns_tc.cu",
+                  "tiled_newton_schulz_03_b300/csrc/ptx.cuh",
+                  "include/himuon.h")
+
+
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "tiled_newton_schulz_03_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + f.read())
     return h.hexdigest()
 
 
