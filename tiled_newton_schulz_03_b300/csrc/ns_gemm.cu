@@ -214,6 +214,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
     }
   } else {
     // ---- epilogue: warps 2..5, TMEM lane quarter = warp % 4, one row per thread
+    {
+      // the global operands of this thread's row (A_bf for G2, X and X_bf for
+      // G3): pulled into L2 while the main loop runs
+      const int64_t rq = m0 + 32 * (warp & 3) + lane;
+      if (MODE == G_POLY) {
+        const char* pa = reinterpret_cast<const char*>(
+            g.ab + static_cast<int64_t>(p) * g.Hp * g.Hp + rq * g.Hp + n0);
+        for (int b = 0; b < BN * 2; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(pa + b));
+      } else if (MODE == G_APPLY) {
+        const int64_t o = static_cast<int64_t>(p) * g.Hp * g.Wp + rq * g.Wp + n0;
+        const char* px = reinterpret_cast<const char*>(g.x32_in + o);
+        const char* pb = reinterpret_cast<const char*>(g.xb_in + o);
+        for (int b = 0; b < BN * 4; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(px + b));
+        for (int b = 0; b < BN * 2; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(pb + b));
+      }
+    }
     // not cut short by an abort: every MMA must finish before TMEM is freed
     wait_drain(ptx::smem_u32(&accf), 0, g.wait_ns, g.err);
     ptx::tc_fence_after();
@@ -226,6 +242,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       const int c0 = n0 + 32 * ch;
+      // G2 / G3: the chunk's global operands are requested before the TMEM
+      // load, so that the two latencies overlap
+      uint4 pre_b[4];
+      float4 pre_x[8];
+      if (MODE == G_POLY) {
+        const uint4* a4 = reinterpret_cast<const uint4*>(g.ab + p * hh + static_cast<int64_t>(r) * g.Hp + c0);
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) pre_b[qd] = a4[qd];
+      } else if (MODE == G_APPLY) {
+        const int64_t off = p * hw + static_cast<int64_t>(r) * g.Wp + c0;
+        const float4* x4 = reinterpret_cast<const float4*>(g.x32_in + off);
+        const uint4* b4 = reinterpret_cast<const uint4*>(g.xb_in + off);
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) pre_b[qd] = b4[qd];
+#pragma unroll
+        for (int qd = 0; qd < 8; ++qd) pre_x[qd] = x4[qd];
+      }
       float v[32];
       ptx::tmem_ld32_sync(taddr + 32 * ch, v);
       if (MODE == G_GRAM) {
@@ -248,11 +281,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
         }
       } else if (MODE == G_POLY) {
         const int64_t off = p * hh + static_cast<int64_t>(r) * g.Hp + c0;
-        const uint4* a4 = reinterpret_cast<const uint4*>(g.ab + off);
         uint4* c4 = reinterpret_cast<uint4*>(g.cb + off);
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
-          const uint4 u = a4[qd];
+          const uint4 u = pre_b[qd];
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
           float w8[8];
 #pragma unroll
@@ -267,15 +299,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
         }
       } else {
         const int64_t off = p * hw + static_cast<int64_t>(r) * g.Wp + c0;
-        const float4* x4 = reinterpret_cast<const float4*>(g.x32_in + off);
-        const uint4* b4 = reinterpret_cast<const uint4*>(g.xb_in + off);
         const float sc = g.step == 0 ? t.s : 1.f;
         float o[32];
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
-          const uint4 u = b4[qd];
+          const uint4 u = pre_b[qd];
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-          const float4 xa = x4[2 * qd], xb = x4[2 * qd + 1];
+          const float4 xa = pre_x[2 * qd], xb = pre_x[2 * qd + 1];
           const float xf[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -378,47 +408,139 @@ __global__ void __launch_bounds__(256) ns_gemm_gather(const GTile* __restrict__ 
   const bool in32 = d.flags & F_IN_FP32, m16 = d.flags & F_M_BF16;
   const int64_t base = (static_cast<int64_t>(p) * Hp + r) * Wp;
   float ss = 0.f;
-  for (int c = lane; c < Wp; c += 32) {
-    float u = 0.f;
-    if (r < ho && c < wo) {
-      const int64_t row = t.tr ? t.i0 + c : t.i0 + r;
-      const int64_t col = t.tr ? t.j0 + r : t.j0 + c;
-      const int64_t gi = row * d.ld_in + col;
-      u = in32 ? static_cast<const float*>(d.in)[gi]
-               : __bfloat162float(static_cast<const __nv_bfloat16*>(d.in)[gi]);
-      if (STEP) {
-        const int64_t mi = row * d.ld_mom + col;
-        const float m = m16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(d.mom)[mi])
-                            : static_cast<const float*>(d.mom)[mi];
-        const float mn = fmaf(st.mu, m, u);
-        if (m16) static_cast<__nv_bfloat16*>(d.mom)[mi] = __float2bfloat16_rn(mn);
-        else static_cast<float*>(d.mom)[mi] = mn;
-        u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
+  // rows of a tile that is not transposed, with 16-byte aligned source rows:
+  // lane l takes 8 consecutive columns at a time (16-byte loads and stores)
+  const bool vec = !t.tr && (d.flags & F_IN_VEC) && (!STEP || (d.flags & F_M_VEC)) &&
+                   (t.j0 % 8 == 0);
+  if (vec) {
+    for (int c = 8 * lane; c < Wp; c += 256) {
+      float u[8];
+      if (r < ho && c + 8 <= wo) {
+        const int64_t gi = static_cast<int64_t>(t.i0 + r) * d.ld_in + t.j0 + c;
+        if (in32) {
+          const float4* g4 = reinterpret_cast<const float4*>(static_cast<const float*>(d.in) + gi);
+          const float4 a = g4[0], b = g4[1];
+          u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w; u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+        } else {
+          const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(d.in) + gi);
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            u[2 * j] = ptx::bf16lo(aw[j]);
+            u[2 * j + 1] = ptx::bf16hi(aw[j]);
+          }
+        }
+        if (STEP) {
+          const int64_t mi = static_cast<int64_t>(t.i0 + r) * d.ld_mom + t.j0 + c;
+          float m[8];
+          if (m16) {
+            const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(d.mom) + mi);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              m[2 * j] = ptx::bf16lo(aw[j]);
+              m[2 * j + 1] = ptx::bf16hi(aw[j]);
+            }
+          } else {
+            const float4* m4 = reinterpret_cast<const float4*>(static_cast<const float*>(d.mom) + mi);
+            const float4 a = m4[0], b = m4[1];
+            m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w; m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float mn = fmaf(st.mu, m[j], u[j]);
+            u[j] = st.nesterov ? fmaf(st.mu, mn, u[j]) : mn;
+            m[j] = mn;
+          }
+          if (m16) {
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(d.mom) + mi) =
+                make_uint4(ptx::pack_bf16x2(m[0], m[1]), ptx::pack_bf16x2(m[2], m[3]),
+                           ptx::pack_bf16x2(m[4], m[5]), ptx::pack_bf16x2(m[6], m[7]));
+          } else {
+            float4* m4 = reinterpret_cast<float4*>(static_cast<float*>(d.mom) + mi);
+            m4[0] = make_float4(m[0], m[1], m[2], m[3]);
+            m4[1] = make_float4(m[4], m[5], m[6], m[7]);
+          }
+        }
+      } else {
+        // the ragged edge of the tile, or padding
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float x = 0.f;
+          if (r < ho && c + j < wo) {
+            const int64_t gi = static_cast<int64_t>(t.i0 + r) * d.ld_in + t.j0 + c + j;
+            x = in32 ? static_cast<const float*>(d.in)[gi]
+                     : __bfloat162float(static_cast<const __nv_bfloat16*>(d.in)[gi]);
+            if (STEP) {
+              const int64_t mi = static_cast<int64_t>(t.i0 + r) * d.ld_mom + t.j0 + c + j;
+              const float m = m16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(d.mom)[mi])
+                                  : static_cast<const float*>(d.mom)[mi];
+              const float mn = fmaf(st.mu, m, x);
+              if (m16) static_cast<__nv_bfloat16*>(d.mom)[mi] = __float2bfloat16_rn(mn);
+              else static_cast<float*>(d.mom)[mi] = mn;
+              x = st.nesterov ? fmaf(st.mu, mn, x) : mn;
+            }
+          }
+          u[j] = x;
+        }
       }
+      float4* x4 = reinterpret_cast<float4*>(x32 + base + c);
+      x4[0] = make_float4(u[0], u[1], u[2], u[3]);
+      x4[1] = make_float4(u[4], u[5], u[6], u[7]);
+      *reinterpret_cast<uint4*>(xb + base + c) =
+          make_uint4(ptx::pack_bf16x2(u[0], u[1]), ptx::pack_bf16x2(u[2], u[3]),
+                     ptx::pack_bf16x2(u[4], u[5]), ptx::pack_bf16x2(u[6], u[7]));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(u[j], u[j], ss);
     }
-    x32[base + c] = u;
-    xb[base + c] = __float2bfloat16_rn(u);
-    ss = fmaf(u, u, ss);
+  } else {
+    for (int c = lane; c < Wp; c += 32) {
+      float u = 0.f;
+      if (r < ho && c < wo) {
+        const int64_t row = t.tr ? t.i0 + c : t.i0 + r;
+        const int64_t col = t.tr ? t.j0 + r : t.j0 + c;
+        const int64_t gi = row * d.ld_in + col;
+        u = in32 ? static_cast<const float*>(d.in)[gi]
+                 : __bfloat162float(static_cast<const __nv_bfloat16*>(d.in)[gi]);
+        if (STEP) {
+          const int64_t mi = row * d.ld_mom + col;
+          const float m = m16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(d.mom)[mi])
+                              : static_cast<const float*>(d.mom)[mi];
+          const float mn = fmaf(st.mu, m, u);
+          if (m16) static_cast<__nv_bfloat16*>(d.mom)[mi] = __float2bfloat16_rn(mn);
+          else static_cast<float*>(d.mom)[mi] = mn;
+          u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
+        }
+      }
+      x32[base + c] = u;
+      xb[base + c] = __float2bfloat16_rn(u);
+      ss = fmaf(u, u, ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) part[static_cast<int64_t>(p) * Hp + r] = ss;
 }
 
-// Normalisation factor of each tile: partials summed in row order.
+// Normalisation factor of each tile, one warp per tile: lane l adds the row
+// partials l, l + 32, ... in order (fp64), and the 32 lane sums are combined
+// in a fixed butterfly order, so the factor does not depend on the batch.
 __global__ void ns_gemm_norm(GTile* __restrict__ tiles, const MatDesc* __restrict__ descs, int n,
                              int Hp, const float* __restrict__ part, int norm, float eps) {
-  const int p = blockIdx.x * blockDim.x + threadIdx.x;
-  if (p >= n) return;
+  const int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= n) return;                      // whole warps
   float s = 1.f;
   if (norm == NORM_TILE) {
     double acc = 0.0;
-    for (int r = 0; r < Hp; ++r) acc += part[static_cast<int64_t>(p) * Hp + r];
+    for (int r = lane; r < Hp; r += 32) acc += part[static_cast<int64_t>(p) * Hp + r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     s = static_cast<float>(1.0 / (sqrt(acc) + static_cast<double>(eps)));
   } else if (norm == NORM_MATRIX) {
     s = descs[tiles[p].mi].norm_scale;
   }
-  tiles[p].s = s;
+  if (lane == 0) tiles[p].s = s;
 }
 
 // K = 0: the output is s U.
@@ -491,7 +613,7 @@ cudaError_t launch_ns_gemm_batch(const GTile* d_tiles, int n, int Hp, int Wp, co
     ns_gemm_gather<true><<<rgrid, 256, 0, stream>>>(tiles, descs, Hp, Wp, x32[0], xb[0], part, st);
   else
     ns_gemm_gather<false><<<rgrid, 256, 0, stream>>>(tiles, descs, Hp, Wp, x32[0], xb[0], part, st);
-  ns_gemm_norm<<<(n + 127) / 128, 128, 0, stream>>>(tiles, descs, n, Hp, part, ns.norm, ns.eps);
+  ns_gemm_norm<<<(n + 3) / 4, 128, 0, stream>>>(tiles, descs, n, Hp, part, ns.norm, ns.eps);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ns.K == 0) {
