@@ -68,8 +68,9 @@ typedef enum {
 } himuon_norm;
 
 typedef enum {
-  HIMUON_PATH_AUTO = 0,    /* bf16 tensor-core path (tcgen05); matrices with
-                              min(H, W) <= 2 or fewer than 4096 elements run on
+  HIMUON_PATH_AUTO = 0,    /* bf16 tensor-core path; matrices with
+                              min(H, W) <= 2 or fewer than 4096 elements, and
+                              tiles of fewer than 64 elements (T < 8), run on
                               the fp32 path (too few elements for the bf16
                               rounding to average out) */
   HIMUON_PATH_TENSOR = 1,  /* same, requested explicitly */
@@ -123,10 +124,11 @@ void himuon_default_ns_params(himuon_ns_params* p);
  * Tiled NS map of one matrix (abstract, sentences 3-5).
  * G: H x W input, ld ldg, dtype gtype (BF16 or FP32).
  * out: H x W output, ld ldo, dtype otype (BF16 or FP32); may be G itself.
- * T: tile size, 1 <= T. The tensor path runs T = 32, 64 and 128 on chip and
- *    every T >= 65 (including 256, and T >= max(H, W): one tile = the
- *    full-matrix map of Muon, sentences 1-2) as batched GEMMs; other T (below 64,
- *    except 32) return HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any T.
+ * T: tile size, 1 <= T. The tensor path runs T <= 32 one tile per warp
+ *    (warp-level MMA), T = 64 and 128 on chip (tcgen05), and every T >= 65
+ *    (including 256, and T >= max(H, W): one tile = the full-matrix map of
+ *    Muon, sentences 1-2) as batched GEMMs; 32 < T < 64 returns
+ *    HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any T.
  * K: number of NS steps, 0 <= K <= 64.
  * params: NULL means the defaults.
  * Returns HIMUON_ERR_INVALID_ARG for H or W < 1, ld < W, NULL pointers, bad

@@ -65,32 +65,35 @@ def test_lowrank_bf16_ragged(H, W, path, T):
     assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
 
 
+@pytest.mark.parametrize("T", [128, 32])
 @pytest.mark.parametrize("K", [0, 1, 3])
 @pytest.mark.parametrize("path", ["tensor", "fp32"])
-def test_small_K(K, path):
+def test_small_K(K, path, T):
     G = synth.lowrank_noise(200, 300, seed=K + 40)
-    out = hm.tiled_ns(G.cuda(), 128, K, path=path, out_dtype=torch.float32)
-    want = oracle.tiled_ns(f64(G), 128, K)
+    out = hm.tiled_ns(G.cuda(), T, K, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, K)
     tol = TOL_BF16 if (path == "tensor" and K > 0) else TOL_FP32
     assert rel_fro(f64(out), want) <= tol
 
 
+@pytest.mark.parametrize("T", [128, 32])
 @pytest.mark.parametrize("norm", ["matrix", "none"])
 @pytest.mark.parametrize("path", ["tensor", "fp32"])
-def test_norm_modes(norm, path):
+def test_norm_modes(norm, path, T):
     G = synth.lowrank_noise(256, 384, seed=5)
     if norm == "none":
         G = (G.float() / G.float().norm() * 0.5).to(torch.bfloat16)   # keep the map stable
-    out = hm.tiled_ns(G.cuda(), 128, 5, norm=norm, path=path, out_dtype=torch.float32)
-    want = oracle.tiled_ns(f64(G), 128, 5, norm=norm)
+    out = hm.tiled_ns(G.cuda(), T, 5, norm=norm, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5, norm=norm)
     assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
 
 
-def test_other_coefficients():
+@pytest.mark.parametrize("T", [128, 32])
+def test_other_coefficients(T):
     G = synth.lowrank_noise(256, 256, seed=8)
     coeffs = (1.5, -0.5, 0.0)
-    out = hm.tiled_ns(G.cuda(), 128, 8, coeffs=coeffs, out_dtype=torch.float32)
-    want = oracle.tiled_ns(f64(G), 128, 8, coeffs)
+    out = hm.tiled_ns(G.cuda(), T, 8, coeffs=coeffs, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 8, coeffs)
     assert rel_fro(f64(out), want) <= TOL_BF16
 
 
@@ -222,6 +225,38 @@ def test_t32_step_and_chunking():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("T", [8, 16, 24])
+@pytest.mark.parametrize("H,W", [(256, 512), (300, 530), (37, 9)])
+def test_tensor_tiles_below_32(H, W, T):
+    """T <= 32 runs one warp per tile, zero-padded to 32 x 32."""
+    G = synth.gaussian(H, W, seed=T + H)
+    out = hm.tiled_ns(G.cuda(), T, 5, path="tensor", out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_auto_path_sends_tiny_tiles_to_fp32(T):
+    """Tiles of fewer than 64 elements: the AUTO path takes the fp32 kernels (a
+    1 x 1 tile on bf16 operands is off by about 2 %)."""
+    G = synth.gaussian(256, 512, seed=T)
+    out = hm.tiled_ns(G.cuda(), T, 5, path="auto", out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
+    assert rel_fro(f64(out), want) <= TOL_FP32
+
+
+def test_t16_step_fp32_weights_bf16_momentum():
+    Ws, Gs, Ms = _step_case([(200, 130), (64, 96)], 97, mdtype=torch.bfloat16, wdtype=torch.float32)
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, 16, 5, lr=0.02, mu=0.95, weight_decay=0.01, path="tensor")
+    for i in range(2):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 16, 5, lr=0.02, mu=0.95,
+                                       weight_decay=0.01)
+        assert rel_fro(f64(Ms[i]), Mn) <= 2.0 ** -8       # bf16 momentum buffer
+        d_gpu, d_ref = f64(Ws[i]) - W0[i], Wn - W0[i]
+        assert np.linalg.norm(d_gpu - d_ref) <= TOL_BF16 * np.linalg.norm(d_ref)
+
+
 def test_step_three_successive_steps_with_tile_schedule():
     shapes = [(1000, 3000 // 4), (2048, 503)]
     Ws, _, Ms = _step_case(shapes, 70)
@@ -323,7 +358,7 @@ def test_bad_arguments_raise_without_launch():
     with pytest.raises(hm.HimuonError):
         hm.tiled_ns(G, 128, 5, out=G[:, :3])
     with pytest.raises(hm.HimuonError) as e:
-        hm.tiled_ns(G, 16, 5, path="tensor")         # no tensor kernel for T = 16
+        hm.tiled_ns(G, 48, 5, path="tensor")         # no tensor kernel for 32 < T < 64
     assert e.value.status_name == "UNSUPPORTED"
     big = torch.zeros(8, 8, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(hm.HimuonError):               # partial overlap of out and G

@@ -286,13 +286,16 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   }
 
   const bool fp32 = p.path == HIMUON_PATH_FP32;
-  // tensor path: T = 64 and 128 run on chip (ns_tc.cu); T > 64 otherwise, and
+  // tensor path: T <= 32 one tile per warp (ns_mma32.cu); T = 64 and 128 on
+  // chip (ns_tc.cu); T > 64 otherwise, and
   // the full-matrix map, run as batched GEMMs (ns_gemm.cu)
-  const bool onchip = T == 32 || T == 64 || T == 128;
-  if (!fp32 && !onchip && T < 64) {
+  // T <= 32: one warp per tile (ns_mma32.cu)
+  const bool warp_tiles = T <= 32;
+  const bool onchip = T == 64 || T == 128;
+  if (!fp32 && !onchip && !warp_tiles && T < 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
-                    " is not implemented in this build; use T = 32 or T >= 64, or the fp32 path");
+                    " is not implemented in this build; use T <= 32 or T >= 64, or the fp32 path");
   }
 
   // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
@@ -395,6 +398,14 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
     return HIMUON_OK;
   }
 
+  if (warp_tiles) {
+    for (auto& c : chunks) {
+      e = launch_ns_mma32(d_descs, n, c.first, c.second, ns, st, h->num_sms, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
+      h->launches += 1;
+    }
+    return HIMUON_OK;
+  }
   if (onchip) {
     for (auto& c : chunks) {
       e = launch_ns_tc(d_descs, d_maps, n, c.first, c.second, ns, st, h->wait_ns, h->d_err,
@@ -407,12 +418,14 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   return run_gemm_path(h, descs, d_descs, T, ns, st, chunks, stream);
 }
 
-// Under HIMUON_PATH_AUTO, matrices this small or thin run on the fp32 path:
-// with so few elements the bf16 rounding of the tensor path does not average
-// out (errors of several percent on rank-1 matrices of a few elements), and a
-// 128-row tensor-core product would be almost all padding anyway.
-bool needs_fp32(const MatDesc& d) {
-  return std::min(d.H, d.W) <= 2 || static_cast<int64_t>(d.H) * d.W < 4096;
+// Under HIMUON_PATH_AUTO, matrices this small or thin, and tiles of fewer than
+// 64 elements, run on the fp32 path: with so few elements per tile the bf16
+// rounding of the tensor path does not average out (errors of several percent
+// on rank-1 matrices of a few elements, about 2 % on 1 x 1 tiles), and a
+// tensor-core product would be almost all padding anyway.
+bool needs_fp32(const MatDesc& d, int32_t T) {
+  const int64_t th = std::min<int64_t>(T, d.H), tw = std::min<int64_t>(T, d.W);
+  return std::min(d.H, d.W) <= 2 || static_cast<int64_t>(d.H) * d.W < 4096 || th * tw < 64;
 }
 
 // Runs the plan, with the small matrices of an AUTO-path request split off to
@@ -422,7 +435,7 @@ himuon_status run_auto(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
                        cudaStream_t stream) {
   if (p.path != HIMUON_PATH_AUTO) return run_plan(h, descs, T, K, p, st, chunk_bytes, stream);
   std::vector<MatDesc> big, small;
-  for (const MatDesc& d : descs) (needs_fp32(d) ? small : big).push_back(d);
+  for (const MatDesc& d : descs) (needs_fp32(d, T) ? small : big).push_back(d);
   if (!big.empty()) {
     himuon_status s = run_plan(h, big, T, K, p, st, chunk_bytes, stream);
     if (s != HIMUON_OK) return s;

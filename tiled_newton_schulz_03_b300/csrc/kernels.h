@@ -20,6 +20,12 @@ cudaError_t launch_ns_tc(const MatDesc* descs, const void* maps, int ndesc, int6
                          int64_t tile_end, const NSArgs& ns, const StepArgs& st, uint64_t wait_ns,
                          int* err, int num_sms, cudaStream_t stream);
 
+// Tensor-core tiled NS for T <= 32 (ns_mma32.cu): one warp per tile, warp-level
+// mma.sync; any alignment, plain loads. Same arguments as launch_ns_tc without
+// the tensor maps and the wait limit (nothing waits on another thread).
+cudaError_t launch_ns_mma32(const MatDesc* descs, int ndesc, int64_t tile_begin, int64_t tile_end,
+                            const NSArgs& ns, const StepArgs& st, int num_sms, cudaStream_t stream);
+
 // fp32 validation path (ns_fp32.cu): tiles (cut at multiples of T) padded to
 // P x P (P = min(T, largest matrix side)) in a scratch buffer of 3 * nb * P * P
 // floats; processes tiles [tile_begin, tile_end) in sub-batches of at most nb
