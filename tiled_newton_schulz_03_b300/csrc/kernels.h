@@ -12,7 +12,7 @@
 
 namespace himuon {
 
-// Tensor-core tiled NS, T in {32, 64, 128} (ns_tc.cu). descs: device array of ndesc
+// Tensor-core tiled NS, T in {64, 128} (ns_tc.cu). descs: device array of ndesc
 // MatDesc; maps: device array of 2 * ndesc CUtensorMap (G, M), 64-byte aligned,
 // valid for matrices flagged F_TMA; tiles [tile_begin, tile_end) of the flat
 // tile list are processed. st.enabled selects the fused HiMuon step.

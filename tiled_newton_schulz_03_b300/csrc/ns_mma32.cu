@@ -147,31 +147,38 @@ __global__ void __launch_bounds__(MTHREADS, 2)
     // issued before any is used.
     float ssq = 0.f;
     {
+      // one predicated read-only load per row, all issued before any is used
+      // (the dtype is chosen once per tile, outside the row loop)
       float u[32];
       const bool col_ok = lane < w;
+      const int hv = col_ok ? h : 0;           // rows this lane loads
+      if (in32) {
+        const float* gp = static_cast<const float*>(d.in) + static_cast<int64_t>(i0) * d.ld_in + j0 + lane;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        u[i] = 0.f;
-        if (i < h && col_ok) {
-          const int64_t gi = static_cast<int64_t>(i0 + i) * d.ld_in + j0 + lane;
-          u[i] = in32 ? static_cast<const float*>(d.in)[gi]
-                      : __bfloat162float(static_cast<const __nv_bfloat16*>(d.in)[gi]);
-        }
+        for (int i = 0; i < 32; ++i) u[i] = (i < hv) ? __ldg(gp + static_cast<int64_t>(i) * d.ld_in) : 0.f;
+      } else {
+        const __nv_bfloat16* gp =
+            static_cast<const __nv_bfloat16*>(d.in) + static_cast<int64_t>(i0) * d.ld_in + j0 + lane;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          u[i] = (i < hv) ? __bfloat162float(__ldg(gp + static_cast<int64_t>(i) * d.ld_in)) : 0.f;
       }
       if (STEP) {
         float m[32];
+        if (m16) {
+          const __nv_bfloat16* mp =
+              static_cast<const __nv_bfloat16*>(d.mom) + static_cast<int64_t>(i0) * d.ld_mom + j0 + lane;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          m[i] = 0.f;
-          if (i < h && col_ok) {
-            const int64_t mo = static_cast<int64_t>(i0 + i) * d.ld_mom + j0 + lane;
-            m[i] = m16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(d.mom)[mo])
-                       : static_cast<const float*>(d.mom)[mo];
-          }
+          for (int i = 0; i < 32; ++i)
+            m[i] = (i < hv) ? __bfloat162float(mp[static_cast<int64_t>(i) * d.ld_mom]) : 0.f;
+        } else {
+          const float* mp = static_cast<const float*>(d.mom) + static_cast<int64_t>(i0) * d.ld_mom + j0 + lane;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m[i] = (i < hv) ? mp[static_cast<int64_t>(i) * d.ld_mom] : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (i < h && col_ok) {
+          if (i < hv) {
             const float mn = fmaf(st.mu, m[i], u[i]);
             const int64_t mo = static_cast<int64_t>(i0 + i) * d.ld_mom + j0 + lane;
             if (m16) static_cast<__nv_bfloat16*>(d.mom)[mo] = __float2bfloat16_rn(mn);

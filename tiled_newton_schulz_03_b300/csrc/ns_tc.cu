@@ -1,4 +1,4 @@
-// Tiled Newton-Schulz on tcgen05 tensor cores, T in {32, 64, 128}: warp-specialised,
+// Tiled Newton-Schulz on tcgen05 tensor cores, T in {64, 128}: warp-specialised,
 // two tile slots per SM, TMA-fed.
 //
 // Method ("Hierarchical Muon: Tiled Newton-Schulz Updates for Efficient Muon
@@ -23,8 +23,8 @@
 // slot's product, the other slot's warps run their epilogue, so the serial
 // chain of a tile's 3K products never leaves the tensor pipe idle for long.
 //
-// A stage is 128 rows: one 128 x 128 tile, or two 64 x 64 (four 32 x 32) tiles
-// stacked vertically (T = 64, 32). With stacked tiles, tile t's products use the whole
+// A stage is 128 rows: one 128 x 128 tile, or two 64 x 64 tiles stacked
+// vertically (T = 64). With stacked tiles, tile t's products use the whole
 // 128-row stack as the A operand and tile t's rows as the B operand; only the
 // accumulator lanes of tile t are kept (the others hold unused cross products).
 //
@@ -323,9 +323,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                  int64_t tile_begin, int64_t tile_end, NSArgs ns, StepArgs st, uint64_t wait_ns,
                  int* __restrict__ err) {
   constexpr int TPS = 128 / T;          // tiles per stage (stacked)
-  constexpr int HALF = T / 2;           // columns per epilogue thread (T = 32: 32, one half only)
-  constexpr int NCH = HALF >= 32 ? HALF / 32 : 1;   // 32-column chunks per epilogue thread
-  static_assert(T == 32 || T == 64 || T == 128, "T");
+  constexpr int HALF = T / 2;           // columns per epilogue thread
+  constexpr int NCH = HALF / 32;        // 32-column chunks per epilogue thread
+  static_assert(T == 64 || T == 128, "T");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl ctl;
@@ -544,9 +544,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int hh = ws >> 2;                 // column half
     const int r = 32 * q + lane;            // stage row = TMEM lane
     const int t = r / T, rl = r % T;
-    const int cbase = T > 32 ? hh * HALF : 0;   // first tile column of this thread
-    // T = 32: a row is one 32-column chunk, done by the first column half alone
-    const int nch = (T > 32 || hh == 0) ? NCH : 0;
+    const int cbase = hh * HALF;            // first tile column of this thread
+    const int nch = NCH;
     const uint32_t sx = sbase + sm_x(s), sc = sbase + sm_c(s);
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t t_a = tbase + lane_off + 256u * s + t * T;           // R_A of my tile
@@ -943,9 +942,6 @@ cudaError_t launch_ns_tc(const MatDesc* descs, const void* maps, int ndesc, int6
   if (ns.T == 64)
     return st.enabled ? launch_t<64, true>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream)
                       : launch_t<64, false>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream);
-  if (ns.T == 32)
-    return st.enabled ? launch_t<32, true>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream)
-                      : launch_t<32, false>(descs, m, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 
