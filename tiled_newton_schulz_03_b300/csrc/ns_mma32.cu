@@ -141,6 +141,26 @@ __global__ void __launch_bounds__(MTHREADS, 2)
     const bool tr = h < w;
     const bool in32 = d.flags & F_IN_FP32, m16 = d.flags & F_M_BF16, out32 = d.flags & F_OUT_FP32;
 
+    // the rows of this warp's next tile (G, and M for a step) into L2 while
+    // this one is processed: lane l takes row l (one 32-element row segment
+    // starts at a multiple of T elements, so it spans at most two lines)
+    if (tile + nwarps < tile_end) {
+      const int64_t nt = tile + nwarps;
+      const MatDesc& dn = descs[find_matrix(descs, ndesc, nt)];
+      const int64_t nlt = nt - dn.tile_start;
+      const int ni0 = static_cast<int>(nlt / dn.tiles_w) * T, nj0 = static_cast<int>(nlt % dn.tiles_w) * T;
+      if (lane < min(T, dn.H - ni0)) {
+        const int es = (dn.flags & F_IN_FP32) ? 4 : 2;
+        const char* gp = static_cast<const char*>(dn.in) + ((ni0 + lane) * dn.ld_in + nj0) * es;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
+        if (STEP) {
+          const int ms = (dn.flags & F_M_BF16) ? 2 : 4;
+          const char* mp = static_cast<const char*>(dn.mom) + ((ni0 + lane) * dn.ld_mom + nj0) * ms;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(mp));
+        }
+      }
+    }
+
     // ---- U = G (or, for a step, the Nesterov/plain momentum direction, with
     // M <- mu M + G written back), row by row, into the shared tile at its
     // processed position; zeros outside the tile. All loads of the tile are
