@@ -99,12 +99,13 @@ def test_other_coefficients(T):
 
 # ---------------------------------------------------------------- bit-exact structure
 
+@pytest.mark.parametrize("T", [128, 32, 256])       # on-chip, warp-tile and GEMM kernels
 @pytest.mark.parametrize("H,W", [(300, 530), (129, 1), (1000, 3000)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_identity_map_is_bit_exact(H, W, dtype):
+def test_identity_map_is_bit_exact(H, W, dtype, T):
     G = synth.gaussian(H, W, seed=3, dtype=dtype).cuda()
     for K, coeffs in ((0, hm.QUINTIC), (3, (1.0, 0.0, 0.0))):
-        out = hm.tiled_ns(G, 128, K, coeffs=coeffs, norm="none", out_dtype=dtype)
+        out = hm.tiled_ns(G, T, K, coeffs=coeffs, norm="none", out_dtype=dtype)
         assert torch.equal(out, G)
 
 
@@ -114,24 +115,27 @@ def test_fp32_in_bf16_out_rounds_once():
     assert torch.equal(out, G.to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("path", ["tensor", "fp32"])
-def test_perturbing_one_tile_leaves_others_bit_identical(path):
+@pytest.mark.parametrize("path,T", [("tensor", 128), ("fp32", 128), ("tensor", 32), ("tensor", 256)])
+def test_perturbing_one_tile_leaves_others_bit_identical(path, T):
     G = synth.lowrank_noise(384, 512, seed=9).cuda()
-    base = hm.tiled_ns(G, 128, 5, path=path)
+    base = hm.tiled_ns(G, T, 5, path=path)
     G2 = G.clone()
-    G2[130:140, 260:300] += 0.01          # tile (1, 2)
-    pert = hm.tiled_ns(G2, 128, 5, path=path)
+    G2[130:140, 260:300] += 0.01          # inside the tiles that hold rows 130-139, cols 260-299
+    pert = hm.tiled_ns(G2, T, 5, path=path)
     mask = torch.ones_like(G, dtype=torch.bool)
-    mask[128:256, 256:384] = False
+    r0, r1 = 130 // T * T, -(-140 // T) * T
+    c0, c1 = 260 // T * T, -(-300 // T) * T
+    mask[r0:r1, c0:c1] = False
     assert torch.equal(base[mask], pert[mask])
     assert not torch.equal(base[~mask], pert[~mask])
 
 
-def test_in_place_equals_out_of_place():
+@pytest.mark.parametrize("T", [128, 32, 256])
+def test_in_place_equals_out_of_place(T):
     G = synth.lowrank_noise(300, 400, seed=10).cuda()
-    ref = hm.tiled_ns(G, 128, 5)
+    ref = hm.tiled_ns(G, T, 5)
     X = G.clone()
-    hm.tiled_ns(X, 128, 5, out=X)
+    hm.tiled_ns(X, T, 5, out=X)
     assert torch.equal(X, ref)
 
 
