@@ -93,10 +93,40 @@ __device__ __forceinline__ void pack_a(const Frag& F, AFrag& A) {
     }
 }
 
-// fp32 value of the bf16 element of A-operand fragments at accumulator position (bm, bn, i)
-__device__ __forceinline__ float a_val(const AFrag& A, int bm, int bn, int i) {
-  const uint32_t r = A[bm][bn >> 1][2 * (bn & 1) + (i >> 1)];
-  return (i & 1) ? ptx::bf16hi(r) : ptx::bf16lo(r);
+// Packed fp32 pairs (one instruction for two adjacent columns, the same
+// roundings as two scalar operations).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// the fp32 values of A-operand register q as a packed pair
+__device__ __forceinline__ uint64_t a_pair(uint32_t r) { return pk2(ptx::bf16lo(r), ptx::bf16hi(r)); }
+// F *= x for the whole fragment set
+__device__ __forceinline__ void scale_frag(Frag& F, float x) {
+  const uint64_t x2 = pk2(x, x);
+#pragma unroll
+  for (int bm = 0; bm < 2; ++bm)
+#pragma unroll
+    for (int bn = 0; bn < 4; ++bn)
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const uint64_t v = mul2(pk2(F[bm][bn][i], F[bm][bn][i + 1]), x2);
+        upk2(v, F[bm][bn][i], F[bm][bn][i + 1]);
+      }
 }
 
 // D = M M^T from M's own A-operand fragments (the B operand of (kb, bn) is row
@@ -246,13 +276,19 @@ __global__ void __launch_bounds__(MTHREADS, 2)
               const int row = 16 * bm + g + 8 * (q & 1), col = 16 * kb + 2 * t + 8 * (q >> 1);
               *reinterpret_cast<uint32_t*>(sx + row * XS + col) = XA[bm][kb][q];
             }
+        {
+          const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
 #pragma unroll
-        for (int bm = 0; bm < 2; ++bm)
+          for (int bm = 0; bm < 2; ++bm)
 #pragma unroll
-          for (int bn = 0; bn < 4; ++bn)
+            for (int bn = 0; bn < 4; ++bn)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              R[bm][bn][i] = fmaf(ns.a, R[bm][bn][i], -e * a_val(XA, bm, bn, i));
+              for (int i = 0; i < 4; i += 2) {
+                const uint64_t xb = a_pair(XA[bm][bn >> 1][2 * (bn & 1) + (i >> 1)]);
+                const uint64_t v = fma2(a2, pk2(R[bm][bn][i], R[bm][bn][i + 1]), mul2(ne2, xb));
+                upk2(v, R[bm][bn][i], R[bm][bn][i + 1]);
+              }
+        }
 
         // ---- A = X_bf X_bf^T  ->  A_bf = bf16(s^2 A)  (or C directly when c = 0)
         Frag D;
@@ -260,29 +296,23 @@ __global__ void __launch_bounds__(MTHREADS, 2)
         const float s2 = (k == 0) ? s * s : 1.f;
         AFrag AB;
         if (has_c) {
-#pragma unroll
-          for (int bm = 0; bm < 2; ++bm)
-#pragma unroll
-            for (int bn = 0; bn < 4; ++bn)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) D[bm][bn][i] *= s2;
+          if (k == 0) scale_frag(D, s2);
           pack_a(D, AB);
           // ---- R_A = A_bf A_bf  ->  C = c A_bf A_bf + b A_bf + e I
           gram(AB, D);
+          const uint64_t c2 = pk2(ns.c, ns.c), b2 = pk2(ns.b, ns.b);
 #pragma unroll
           for (int bm = 0; bm < 2; ++bm)
 #pragma unroll
             for (int bn = 0; bn < 4; ++bn)
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                D[bm][bn][i] = fmaf(ns.c, D[bm][bn][i], ns.b * a_val(AB, bm, bn, i));
+              for (int i = 0; i < 4; i += 2) {
+                const uint64_t ab = a_pair(AB[bm][bn >> 1][2 * (bn & 1) + (i >> 1)]);
+                const uint64_t v = fma2(c2, pk2(D[bm][bn][i], D[bm][bn][i + 1]), mul2(b2, ab));
+                upk2(v, D[bm][bn][i], D[bm][bn][i + 1]);
+              }
         } else {
-#pragma unroll
-          for (int bm = 0; bm < 2; ++bm)
-#pragma unroll
-            for (int bn = 0; bn < 4; ++bn)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) D[bm][bn][i] *= ns.b * s2;
+          scale_frag(D, ns.b * s2);
         }
 #pragma unroll
         for (int bm = 0; bm < 2; ++bm) {
@@ -305,14 +335,7 @@ __global__ void __launch_bounds__(MTHREADS, 2)
             mma16816(R[bm][bn], AB[bm][1], b10, b11);
           }
         }
-        if (k == 0) {                         // X_1 = s (C U_bf + a U - e U_bf)
-#pragma unroll
-          for (int bm = 0; bm < 2; ++bm)
-#pragma unroll
-            for (int bn = 0; bn < 4; ++bn)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) R[bm][bn][i] *= s;
-        }
+        if (k == 0) scale_frag(R, s);         // X_1 = s (C U_bf + a U - e U_bf)
         __syncwarp();                         // the shared X_bf is rewritten next step
       }
       // the result into the shared tile (processed coordinates)
