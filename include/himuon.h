@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
   HIMUON_OK = 0,
   HIMUON_ERR_INVALID_ARG = 1,   /* bad size, pointer, ld, T, K or enum value */
-  HIMUON_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  HIMUON_ERR_UNSUPPORTED = 2,   /* valid request this library does not implement */
   HIMUON_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
   HIMUON_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out */
   HIMUON_ERR_NO_DEVICE = 5,     /* no usable sm_103 device */

@@ -295,7 +295,7 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   if (!fp32 && !onchip && !warp_tiles && T < 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
-                    " is not implemented in this build; use T <= 32 or T >= 64, or the fp32 path");
+                    " is not implemented by this library; use T <= 32 or T >= 64, or the fp32 path");
   }
 
   // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
