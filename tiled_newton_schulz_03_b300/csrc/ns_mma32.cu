@@ -113,7 +113,7 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
-// the fp32 values of A-operand register q as a packed pair
+// the two bf16 values of an A-operand register, as a packed fp32 pair
 __device__ __forceinline__ uint64_t a_pair(uint32_t r) { return pk2(ptx::bf16lo(r), ptx::bf16hi(r)); }
 // F *= x for the whole fragment set
 __device__ __forceinline__ void scale_frag(Frag& F, float x) {
@@ -193,12 +193,11 @@ __global__ void __launch_bounds__(MTHREADS, 2)
 
     // ---- U = G (or, for a step, the Nesterov/plain momentum direction, with
     // M <- mu M + G written back), row by row, into the shared tile at its
-    // processed position; zeros outside the tile. All loads of the tile are
-    // issued before any is used.
+    // processed position; zeros outside the tile.
     float ssq = 0.f;
     {
-      // one predicated read-only load per row, all issued before any is used
-      // (the dtype is chosen once per tile, outside the row loop)
+      // one predicated read-only load per row, all issued before any is used;
+      // the dtype is chosen once per tile, outside the row loop
       float u[32];
       const bool col_ok = lane < w;
       const int hv = col_ok ? h : 0;           // rows this lane loads
