@@ -235,9 +235,11 @@ himuon_status himuon_wait_selftest(himuon_handle* handle, void* stream);
  * first call before any stream capture on the device.
  * Concurrency: all calls share the one array, whose contents persist from
  * call to call (nothing in it needs clearing: each call writes every byte it
- * reads before reading it). Calls whose work overlaps on the GPU -- on
- * different streams, or from different host threads -- race on the array and
- * give wrong results; issue them on one stream or serialise them.
+ * reads before reading it). Calls whose work overlaps on the GPU race on the
+ * array and give wrong results: issue them on one stream. A call enqueues a
+ * descriptor upload and then its kernels, so two host threads calling at the
+ * same time can interleave those on one stream as well; a caller with several
+ * host threads must serialise the calls itself, on the host.
  * Asynchronous on `stream` like the other calls.
  */
 himuon_status himuon_tiled_ns_fp32_noalloc(const void* G, int64_t H, int64_t W,

@@ -306,3 +306,59 @@ def test_ema_momentum_gives_same_direction_up_to_eps():
     O1 = oracle.tiled_ns(G, 4, 5, eps=0.0)
     O2 = oracle.tiled_ns(0.05 * G, 4, 5, eps=0.0)
     np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-11)
+
+
+# -- which quantity the step hands to the NS map ----------------------------------
+# With mu != 0, M0 != 0 and no normalisation, the Nesterov input U = G + mu M_new
+# and the plain-momentum input M_new differ, so passing the wrong one (or G, or
+# M0) to the NS map changes O. All values below are exact rationals.
+
+def _p1(x: Fraction) -> Fraction:
+    return p_exact(x, 1, QUINTIC)
+
+
+@pytest.mark.parametrize("nesterov,u", [(True, Fraction(7, 4)), (False, Fraction(3, 2))])
+def test_step_ns_input_hand_value_1x1(nesterov, u):
+    # G = 1, M0 = 1, mu = 1/2: M_new = 3/2; U = 1 + 3/4 = 7/4 (Nesterov) or 3/2.
+    W0, lr = 0.25, 0.125
+    W1, M1, O = oracle.himuon_step(np.array([[W0]]), np.array([[1.0]]), np.array([[1.0]]), 1, 1,
+                                   lr=lr, mu=0.5, nesterov=nesterov, norm="none")
+    assert M1[0, 0] == 1.5
+    want_o = _p1(u)
+    assert abs(O[0, 0] - float(want_o)) <= 1e-12 * abs(float(want_o))
+    want_w = Fraction(W0) - Fraction(lr) * want_o          # s = sqrt(max(1, 1/1)) = 1
+    assert abs(W1[0, 0] - float(want_w)) <= 1e-12 * abs(float(want_w))
+    # the other readings give other values: the pin separates them
+    for wrong in (Fraction(3, 2) if nesterov else Fraction(7, 4), Fraction(1)):
+        assert abs(float(_p1(wrong)) - float(want_o)) > 0.1
+
+
+def test_step_ns_input_scale_and_decay_hand_value_2x1():
+    # A 2 x 1 matrix (H / W = 2, so s = sqrt(2)) with U = [7/4, 0]^T: the
+    # Gram is diag(49/16, 0), so one step maps 7/4 to p(7/4) and 0 to 0.
+    W0 = np.array([[0.5], [-0.25]])
+    G = np.array([[1.0], [0.0]])
+    M0 = np.array([[1.0], [0.0]])
+    lr, wd = 0.125, 0.5
+    W1, M1, O = oracle.himuon_step(W0, G, M0, 2, 1, lr=lr, mu=0.5, nesterov=True,
+                                   weight_decay=wd, norm="none")
+    po = float(_p1(Fraction(7, 4)))
+    np.testing.assert_allclose(O[:, 0], [po, 0.0], rtol=1e-12, atol=0)
+    np.testing.assert_array_equal(M1[:, 0], [1.5, 0.0])
+    s = np.sqrt(2.0)
+    want = W0[:, 0] - lr * wd * W0[:, 0] - lr * s * np.array([po, 0.0])
+    np.testing.assert_allclose(W1[:, 0], want, rtol=1e-13, atol=0)
+
+
+def test_step_ns_input_with_tile_norm_is_direction_of_u():
+    # Per-tile normalisation removes the length of U but not its direction:
+    # on a 1 x 2 tile U = G + mu (mu M0 + G) with G = [1, 0], M0 = [0, 4],
+    # mu = 1/2 gives M_new = [1, 2] and U = [1, 0] + [1/2, 1] = [3/2, 1].
+    G = np.array([[1.0, 0.0]])
+    M0 = np.array([[0.0, 4.0]])
+    _, M1, O = oracle.himuon_step(np.zeros((1, 2)), G, M0, 2, 1, lr=0.0, mu=0.5, eps=0.0)
+    np.testing.assert_array_equal(M1, [[1.0, 2.0]])
+    u = np.array([1.5, 1.0])
+    n = np.linalg.norm(u)
+    # a rank-1 row: the NS step acts on its one singular value 1 after normalising
+    np.testing.assert_allclose(O[0], u / n * float(_p1(Fraction(1))), rtol=1e-12, atol=0)
