@@ -6,11 +6,19 @@ synthetic low-rank-plus-noise gradients resident in HBM.
 
 Prints one JSON line. ``value`` is the algorithmic NS throughput of the whole job
 (6 H W T K flops per matrix per step, summed, over the step time), in TFLOP/s;
-``ms_per_step`` is the optimizer-step time. ``--impl reference`` times the fp64
-CPU oracle on a bounded sample of the same workload instead.
+``ms_per_step`` is the optimizer-step time. ``roofline`` compares the step with
+the slower of its tensor time (6 H W T K at the bf16 dense peak) and its HBM
+time (the bytes of G, M and W read and written once at the measured copy
+bandwidth). ``secondary`` holds the other workloads measured in the same run
+(GPT-2-small set, 4096^2 tile-size sweep, ragged shapes with the runtime tile
+schedule), each with its own roofline, clocks and CPU baseline.
 
-Launch: ``python bench.py [--gpus 1 --steps K --warmup W]``; for N > 1 under
-``torch.distributed.run`` every rank runs the full layer set on its own GPU
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload instead.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``. With N > 1 and no
+torchrun environment the script starts N ranks itself through
+``torch.distributed.run``; every rank runs the full layer set on its own GPU
 (independent replicas, weak scaling, no collective on the data path).
 """
 
@@ -20,6 +28,7 @@ import argparse
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -35,11 +44,19 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL = "ns_tc_kernel"
 
+# Fused step bytes per parameter: G bf16 read (2), M fp32 read + write (8),
+# W bf16 read + write (4).
+STEP_BYTES_PER_PARAM = 14
+
 WORKLOADS = {
     # name: (shapes fn, rank of the synthetic gradients, T, K, chunk bytes)
     "llama3_8b": ("llama3_8b_shapes", 16, 128, 5, 8 << 30),
     "gpt2_small": ("gpt2_small_shapes", 8, 128, 5, 0),
 }
+
+# The CPU baseline's sample, the same in both arms: one fused step of the
+# oracle on one K-projection-shaped matrix (1024 x 4096, 256 tiles of T = 128).
+CPU_SAMPLE_SHAPE = (1024, 4096)
 
 
 def env_int(name, default):
@@ -82,6 +99,19 @@ def dist_max(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def relaunch_command(argv, nproc: int, port: int):
+    """The torchrun command line that starts ``nproc`` ranks of this script."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={nproc}", "--master-addr=127.0.0.1", f"--master-port={port}",
+            os.path.abspath(__file__), *argv]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 # ---------------------------------------------------------------- measurement helpers
 
 def load_peaks():
@@ -92,6 +122,30 @@ def load_peaks():
         return p, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline(flops: float, nbytes: float, seconds: float, peaks, peak_src: str) -> dict:
+    """Roofline of a measured region: the slower of the tensor time (flops at
+    the burst bf16 peak) and the HBM time (bytes at the copy bandwidth) sets
+    the bound; ``frac`` = that time / the measured time."""
+    p_tc = float(peaks.get("bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"])
+    p_hbm = float(peaks.get("hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"])
+    t_tc = flops / (p_tc * 1e12)
+    t_hbm = nbytes / (p_hbm * 1e9)
+    if t_tc >= t_hbm:
+        r = {"bound": "tensor", "achieved": round(flops / seconds / 1e12, 2), "peak": p_tc,
+             "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": round(nbytes / seconds / 1e9, 1), "peak": p_hbm,
+             "unit": "GB/s"}
+    r["frac"] = round(r["achieved"] / r["peak"], 4)
+    r["roofline_ms"] = round(max(t_tc, t_hbm) * 1e3, 4)
+    r["tensor_ms"] = round(t_tc * 1e3, 4)
+    r["hbm_ms"] = round(t_hbm * 1e3, 4)
+    r["algorithmic_flops"] = flops
+    r["algorithmic_bytes"] = nbytes
+    r["peak_source"] = f"{peak_src}: bf16_tflops (burst) and hbm_gbs of MEASURED_PEAKS.json"
+    return r
 
 
 class ClockSampler:
@@ -190,45 +244,63 @@ def workload_shapes(name):
 
 
 def step_flops(shapes, T, K):
-    return sum(6.0 * H * W * T * K for H, W in shapes)
+    return sum(6.0 * H * W * min(T, max(H, W)) * K for H, W in shapes)
 
 
-def cpu_oracle_rate(shapes, T, K, budget_s: float, max_tiles: int | None = None):
-    """Times the fp64 oracle's fused step on whole sample matrices of the
-    workload until ``budget_s`` seconds of CPU work have run. Returns
-    (flops/s, description, threads)."""
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_oracle_step(H, W, T, K, seed, rank=16):
+    """One fused step of the fp64 oracle on one seeded H x W matrix; returns
+    (seconds, flops)."""
     import numpy as np
-    import torch
 
     import oracle
     from tiled_newton_schulz_03_b300 import synth
 
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
-    except Exception:
-        threads = os.cpu_count()
-    # sample: the K-projection shape (1024 x 4096), or a row band of a matrix
-    H, W = min(shapes, key=lambda s: s[0] * s[1])
-    rows = H
-    if max_tiles is not None:
-        rows = max(T, min(H, (max_tiles // max(1, math.ceil(W / T))) * T))
-    done_flops, spent, n = 0.0, 0.0, 0
-    while spent < budget_s or n == 0:
-        G = synth.lowrank_noise(rows, W, seed=900 + n, rank=16).double().numpy()
-        Wt = synth.gaussian(rows, W, seed=950 + n, std=0.02).double().numpy()
-        M = np.zeros((rows, W))
-        t0 = time.perf_counter()
-        oracle.himuon_step(Wt, G, M, T, K, lr=0.02, mu=0.95)
-        spent += time.perf_counter() - t0
-        done_flops += 6.0 * rows * W * T * K
+    G = synth.lowrank_noise(H, W, seed=seed, rank=rank).double().numpy()
+    Wt = synth.gaussian(H, W, seed=seed + 50, std=0.02).double().numpy()
+    M = np.zeros((H, W))
+    t0 = time.perf_counter()
+    oracle.himuon_step(Wt, G, M, T, K, lr=0.02, mu=0.95)
+    return time.perf_counter() - t0, 6.0 * H * W * min(T, max(H, W)) * K
+
+
+def cpu_oracle_ns(H, W, T, K, seed, rank=8):
+    """The oracle's tiled NS map (or, for T >= max(H, W), the full-matrix map)
+    on one seeded H x W matrix; returns (seconds, flops)."""
+    import oracle
+    from tiled_newton_schulz_03_b300 import synth
+
+    G = synth.lowrank_noise(H, W, seed=seed, rank=rank).double().numpy()
+    t0 = time.perf_counter()
+    if T >= max(H, W):
+        oracle.full_ns(G, K)
+    else:
+        oracle.tiled_ns(G, T, K)
+    return time.perf_counter() - t0, 6.0 * H * W * min(T, max(H, W)) * K
+
+
+def cpu_baseline(fn, budget_s: float, desc: str, min_runs: int = 1):
+    """Repeats ``fn(i) -> (seconds, flops)`` until budget_s of CPU work has run."""
+    spent, flops, n = 0.0, 0.0, 0
+    while n < min_runs or spent < budget_s:
+        s, f = fn(n)
+        spent += s
+        flops += f
         n += 1
-        if max_tiles is not None:
-            break
-    del torch
-    desc = (f"{n} x fused step of one {rows}x{W} matrix ({rows * W // (T * T)} tiles of "
-            f"T={T}, K={K}) in fp64, {spent:.1f} s")
-    return done_flops / spent, desc, threads, spent
+    return {"value": round(flops / spent / 1e12, 6), "unit": UNIT, "cores": oracle_threads(),
+            "kind": "oracle", "sample": f"{n} x {desc} in fp64 ({spent:.1f} s)"}, flops / spent
+
+
+def headline_cpu_sample(i, T=128, K=5):
+    H, W = CPU_SAMPLE_SHAPE
+    return cpu_oracle_step(H, W, T, K, seed=900 + i)
 
 
 # ---------------------------------------------------------------- our implementation
@@ -249,6 +321,7 @@ def run_ours(args):
     shapes, grank, T, K, chunk = workload_shapes(args.workload)
     flops = step_flops(shapes, T, K)
     nparams = sum(H * W for H, W in shapes)
+    nbytes = nparams * STEP_BYTES_PER_PARAM
 
     # inputs resident in HBM: G bf16 (low-rank + noise), W bf16 ~ N(0, 0.02^2), M fp32 = 0
     Gs = [synth.lowrank_noise(H, W, seed=1000 * rank + i, rank=grank, device=dev)
@@ -289,24 +362,32 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
-    # roofline of the fused step kernel: its launches are back to back on the
-    # stream and make up the step; achieved = step flops / step time.
+    # Roofline of the fused step kernel. Its launches run back to back on the
+    # stream and are the whole step (ncu launch list), so the average launch
+    # duration is the step time / launches per step, and per launch the
+    # algorithmic work is the step's / launches per step: the ratio is the same.
     launches_per_step = launches / args.steps
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops_sustained"])
-    achieved = flops / (statistics.median(step_ms) * 1e-3) / 1e12
+    med_s = statistics.median(step_ms) * 1e-3
+    roof = roofline(flops, nbytes, med_s, peaks, peak_src)
     traffic_info = ncu_traffic(kernel_source_hash())
     traffic = None
     if traffic_info and traffic_info.get("workload") == args.workload:
         traffic = traffic_info.get("dram_bytes_per_launch")
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_kind": f"bf16_tflops_sustained ({peak_src})",
-                "frac_of_burst": round(achieved / float(peaks.get("bf16_tflops") or 1800.0), 4),
-                "kernel": KERNEL + "<step>", "launches_per_step": launches_per_step,
-                "hbm_bytes_per_step_algorithmic": nparams * (2 + 8 + 4),
-                "hbm_frac_of_step": round(nparams * 14 / (statistics.median(step_ms) * 1e-3) /
-                                          (float(peaks.get("hbm_gbs") or 6400.0) * 1e9), 4)}
+    roof.update({
+        "traffic": traffic, "kernel": KERNEL + "<128, step>",
+        "launches_per_step": launches_per_step,
+        "launch_ms_avg": round(statistics.median(step_ms) / max(launches_per_step, 1), 3),
+        "algorithmic_bytes_per_launch": nbytes / max(launches_per_step, 1),
+        "bytes_per_param": STEP_BYTES_PER_PARAM,
+        "hbm_frac": round(roof["hbm_ms"] / (med_s * 1e3), 4),
+        "tensor_frac": round(roof["tensor_ms"] / (med_s * 1e3), 4),
+        "tensor_frac_of_sustained_peak": round(
+            flops / med_s / 1e12 / float(peaks.get("bf16_tflops_sustained") or 1400.0), 4),
+        "sustained_peak_note": "bf16_tflops_sustained was taken at a median SM clock of "
+                               f"{peaks.get('clocks_under_load', {}).get('sm_mhz_median')} MHz "
+                               "(cuBLAS under the power cap); reported for context only",
+    })
 
     # end to end through the public API: G from pinned host memory, step, W back
     e2e = None
@@ -315,9 +396,17 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, threads, _ = cpu_oracle_rate(shapes, T, K, args.cpu_seconds)
-        cpu = {"value": round(rate / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": desc, "ms_per_step_extrapolated": round(flops / rate * 1e3, 1)}
+        H, W = CPU_SAMPLE_SHAPE
+        cpu, rate = cpu_baseline(headline_cpu_sample, args.cpu_seconds,
+                                 f"fused step of one {H}x{W} matrix ({H * W // (T * T)} tiles of "
+                                 f"T={T}, K={K})")
+        cpu["ms_per_step_extrapolated_full_workload"] = round(flops / rate * 1e3, 1)
+
+    secondary = None
+    if rank == 0 and world == 1 and args.secondary and args.workload == "llama3_8b":
+        del Gs, Ws, Ms
+        torch.cuda.empty_cache()
+        secondary = run_secondary(hm, handle, dev, stream, peaks, peak_src, args)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -329,19 +418,26 @@ def run_ours(args):
                    "T": T, "K": K, "matrices": len(shapes), "params": nparams,
                    "chunk_bytes": chunk, "grad_dtype": "bf16", "weight_dtype": "bf16",
                    "momentum_dtype": "fp32", "l2": "inputs larger than L2 (G+M+W = "
-                   f"{nparams * 14 / 1e9:.0f} GB per step)",
+                   f"{nbytes / 1e9:.0f} GB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
                     "max": round(max(step_ms), 3)},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
     }
+    if secondary is not None:
+        line["secondary"] = secondary
     if rank == 0:
         print(json.dumps(line), flush=True)
     handle.close()
 
 
 def run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, world, dev):
+    """The same step through the public API with the gradients coming from, and
+    the weights going back to, pinned host memory every step. Layers are
+    pipelined: layer l's gradients go up on one copy stream while layer l-1 is
+    stepped on the compute stream and layer l-2's weights come down on another
+    copy stream (events order each layer's copy, step and read-back)."""
     import torch
     try:
         hG = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in Gs]
@@ -353,14 +449,36 @@ def run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, wo
     h2d = sum(g.numel() * g.element_size() for g in Gs)
     d2h = sum(w.numel() * w.element_size() for w in Ws)
     n = max(1, args.e2e_steps)
+    per = max(1, len(Gs) // 32)           # one group per layer of the layer set
+    groups = [list(range(i, min(len(Gs), i + per))) for i in range(0, len(Gs), per)]
+    up = torch.cuda.Stream(dev)
+    down = torch.cuda.Stream(dev)
 
     def e2e_step():
-        for h, g in zip(hG, Gs):
-            g.copy_(h, non_blocking=True)
-        hm.step(Ws, Gs, Ms, T, K, lr=0.02, mu=0.95, nesterov=True, chunk_bytes=chunk,
-                handle=handle, stream=stream)
-        for h, w in zip(hW, Ws):
-            h.copy_(w, non_blocking=True)
+        uploaded = []
+        for gi, idx in enumerate(groups):
+            with torch.cuda.stream(up):
+                for i in idx:
+                    Gs[i].copy_(hG[i], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(up)
+            uploaded.append(e)
+        stepped = []
+        for gi, idx in enumerate(groups):
+            stream.wait_event(uploaded[gi])
+            hm.step([Ws[i] for i in idx], [Gs[i] for i in idx], [Ms[i] for i in idx], T, K,
+                    lr=0.02, mu=0.95, nesterov=True, chunk_bytes=chunk, handle=handle,
+                    stream=stream)
+            e = torch.cuda.Event()
+            e.record(stream)
+            stepped.append(e)
+        for gi, idx in enumerate(groups):
+            down.wait_event(stepped[gi])
+            with torch.cuda.stream(down):
+                for i in idx:
+                    hW[i].copy_(Ws[i], non_blocking=True)
+        # the next step's uploads overwrite G: they wait for this step's kernels
+        up.wait_event(stepped[-1])
 
     e2e_step()
     torch.cuda.synchronize()
@@ -372,112 +490,97 @@ def run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, wo
     dt = dist_max(time.perf_counter() - t0, world, dev)
     return {"value": round(world * flops * n / dt / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(dt / n * 1e3, 2), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n}
-
-
-# ---------------------------------------------------------------- reference arm: the oracle
-
-def run_reference(args):
-    rank, world, _ = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
-    if rank != 0:
-        return
-    shapes, grank, T, K, chunk = workload_shapes(args.workload)
-    flops = step_flops(shapes, T, K)
-    nparams = sum(H * W for H, W in shapes)
-    # each step: the oracle's fused step on a bounded sample (a row band of
-    # the smallest matrix shape, <= 64 tiles); warm-up steps untimed.
-    for _ in range(args.warmup):
-        cpu_oracle_rate(shapes, T, K, 0.0, max_tiles=16)
-    rates, spent, desc, threads = [], 0.0, "", 1
-    for _ in range(args.steps):
-        r, desc, threads, s = cpu_oracle_rate(shapes, T, K, 0.0, max_tiles=64)
-        rates.append(r)
-        spent += s
-    rate = len(rates) / sum(1.0 / r for r in rates)    # total flops / total time
-    value = rate / 1e12
-    line = {
-        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(flops / rate * 1e3, 1), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded low-rank + noise gradients)",
-        "config": {"workload": f"{args.workload}: {len(shapes)} matrices, {nparams / 1e9:.2f} G params, "
-                               f"T={T}, K={K}, fused momentum(0.95, Nesterov) + update(lr 0.02)",
-                   "T": T, "K": K, "matrices": len(shapes), "params": nparams,
-                   "parallelism": "host cores"},
-        "impl": "reference",
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"per step: {desc}; ms_per_step extrapolated to the full "
-                                   f"workload by flops ({spent:.1f} s total)"},
-        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+            "d2h_bytes_per_step": d2h, "steps": n,
+            "pipeline": f"{len(groups)} layer groups; H2D, step and D2H on three streams"}
 
 
 # ---------------------------------------------------------------- secondary workloads
 
-def _timed(fn, reps, flush, stream):
-    """Median CUDA-event time (ms) of fn over reps runs, L2 flushed before each."""
+def _timed(fn, reps, stream, flush=None):
+    """CUDA-event times (ms) of fn over reps runs; L2 flushed before each when
+    the inputs would fit in it."""
     import torch
     times = []
     for _ in range(reps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         fn()
         e.record(stream)
         torch.cuda.synchronize()
         times.append(s.elapsed_time(e))
-    return statistics.median(times)
+    return times
 
 
-def run_sweep(args):
-    """Tile-size sweep on one 4096 x 4096 bf16 matrix (rank-8 + noise), K = 5:
-    tiled NS only, one JSON line per T (T = 4096 is the full-matrix map). The
-    matrix fits in L2, so L2 is flushed (a 256 MB write) before every run."""
+def run_secondary(hm, handle, dev, stream, peaks, peak_src, args):
+    """Configs measured besides the headline: the GPT-2-small fused step, the
+    4096 x 4096 tile-size sweep (tiled NS only) and the ragged set with the
+    runtime tile schedule. Each entry carries its roofline, the clocks seen
+    while it ran, its kernel launches and an oracle CPU baseline on a sample."""
     import torch
 
-    import tiled_newton_schulz_03_b300 as hm
-    from tiled_newton_schulz_03_b300 import build as hbuild, synth
-    hbuild.build()
-    dev = torch.device("cuda", 0)
-    handle = hm.Handle(dev)
-    stream = torch.cuda.current_stream(dev)
+    from tiled_newton_schulz_03_b300 import synth
+    out = []
+    reps = max(5, args.secondary_reps)
+    cpu_s = args.secondary_cpu_seconds
+
+    # ---- GPT-2-small set, fused step, T = 128, K = 5
+    shapes = synth.gpt2_small_shapes()
+    Ws = [synth.gaussian(H, W, seed=10 + i, std=0.02, dtype=torch.bfloat16, device=dev) for i, (H, W) in enumerate(shapes)]
+    Gs = [synth.lowrank_noise(H, W, seed=1 + 100 * i, rank=8, device=dev) for i, (H, W) in enumerate(shapes)]
+    Ms = [torch.zeros(H, W, device=dev) for H, W in shapes]
+    fn = lambda: hm.step(Ws, Gs, Ms, 128, 5, lr=0.02, mu=0.95, handle=handle, stream=stream)
+    for _ in range(args.warmup):
+        fn()
+    with ClockSampler(dev.index) as clk:
+        l0 = handle.launch_count()
+        times = _timed(fn, reps * 8, stream)
+        launches = handle.launch_count() - l0
+    ms = statistics.median(times)
+    nparams = sum(H * W for H, W in shapes)
+    flops = step_flops(shapes, 128, 5)
+    cpu, _ = cpu_baseline(lambda i: cpu_oracle_step(768, 768, 128, 5, seed=40 + i, rank=8), cpu_s,
+                          "fused step of one 768x768 matrix (36 tiles of T=128, K=5)")
+    out.append({"workload": f"gpt2_small: {len(shapes)} matrices, {nparams / 1e6:.1f} M params, "
+                            "T=128, K=5, fused momentum(0.95, Nesterov) + update(lr 0.02)",
+                "ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+                "unit": UNIT, "l2": f"inputs larger than L2 ({nparams * 14 / 1e9:.2f} GB per step)",
+                "roofline": roofline(flops, nparams * STEP_BYTES_PER_PARAM, ms * 1e-3, peaks, peak_src),
+                "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
+                "cpu_baseline": cpu})
+    del Ws, Gs, Ms
+
+    # ---- 4096 x 4096 sweep, tiled NS only (bf16 in and out), K = 5
     G = synth.lowrank_noise(4096, 4096, seed=3, rank=8, device=dev)
-    out = torch.empty_like(G)
-    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
-    peaks, src = load_peaks()
+    o = torch.empty_like(G)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)   # 256 MB > L2
     for T in (32, 64, 128, 256, 4096):
-        fn = lambda: hm.tiled_ns(G, T, 5, out=out, handle=handle, stream=stream)
+        fn = lambda: hm.tiled_ns(G, T, 5, out=o, handle=handle, stream=stream)
         for _ in range(args.warmup):
             fn()
-        ms = _timed(fn, args.steps, flush, stream)
+        with ClockSampler(dev.index) as clk:
+            l0 = handle.launch_count()
+            times = _timed(fn, reps * 4, stream, flush)
+            launches = handle.launch_count() - l0
+        ms = statistics.median(times)
         flops = 6.0 * 4096 * 4096 * min(T, 4096) * 5
-        tf = flops / (ms * 1e-3) / 1e12
-        hbm_ms = 4.0 * 4096 * 4096 / (float(peaks.get("hbm_gbs", 6400.0)) * 1e9) * 1e3
-        print(json.dumps({"workload": "sweep4096", "T": T, "K": 5, "ms": round(ms, 4),
-                          "tflops": round(tf, 2), "frac_of_burst_bf16": round(tf / float(peaks.get("bf16_tflops", 1800.0)), 4),
-                          "roofline_ms": round(max(flops / (float(peaks.get("bf16_tflops", 1800.0)) * 1e12) * 1e3, hbm_ms), 4),
-                          "peak_source": src}), flush=True)
-    assert hm.device_error(handle=handle) == 0
-    handle.close()
+        Hs = 1024 if T == 4096 else 512
+        cpu, _ = cpu_baseline(lambda i: cpu_oracle_ns(Hs, 4096 if T != 4096 else Hs, T, 5, seed=70 + i),
+                              cpu_s, (f"full-matrix map of one {Hs}x{Hs} matrix" if T == 4096 else
+                                      f"tiled map of a {Hs}x4096 row band (T={T})") + ", K=5")
+        out.append({"workload": f"sweep4096: one 4096x4096 bf16 matrix, T={T}, K=5, tiled NS "
+                                "(bf16 out)" + (" = full-matrix map" if T == 4096 else ""),
+                    "T": T, "ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+                    "unit": UNIT, "l2": "flushed before every run (256 MB write)",
+                    "roofline": roofline(flops, 4.0 * 4096 * 4096, ms * 1e-3, peaks, peak_src),
+                    "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
+                    "cpu_baseline": cpu})
+    del G, o, flush
 
-
-def run_ragged(args):
-    """Ragged shapes and the runtime tile schedule: 1000x3000, 5120x13824 and
-    2048x50257 bf16 (rank-8 + noise), three successive fused steps with T = 64,
-    128, 256, for K = 3 and 5; one JSON line per (K, step)."""
-    import torch
-
-    import tiled_newton_schulz_03_b300 as hm
-    from tiled_newton_schulz_03_b300 import build as hbuild, synth
-    hbuild.build()
-    dev = torch.device("cuda", 0)
-    handle = hm.Handle(dev)
-    stream = torch.cuda.current_stream(dev)
+    # ---- ragged set, three fused steps with T = 64 -> 128 -> 256, K = 3 and 5
     shapes = [(1000, 3000), (5120, 13824), (2048, 50257)]
-    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    nparams = sum(H * W for H, W in shapes)
     sched = hm.TSchedule([(0, 64), (1, 128), (2, 256)])
     for K in (3, 5):
         Ws = [synth.gaussian(H, W, seed=10 + i, std=0.02, dtype=torch.bfloat16, device=dev) for i, (H, W) in enumerate(shapes)]
@@ -491,34 +594,128 @@ def run_ragged(args):
             fn = lambda: hm.step(Wc, Gs, Mc, T, K, lr=0.02, mu=0.95, handle=handle, stream=stream)
             for _ in range(args.warmup):
                 fn()
-            ms = _timed(fn, args.steps, flush, stream)
+            with ClockSampler(dev.index) as clk:
+                l0 = handle.launch_count()
+                times = _timed(fn, reps, stream)
+                launches = handle.launch_count() - l0
             hm.step(Ws, Gs, Ms, T, K, lr=0.02, mu=0.95, handle=handle, stream=stream)
-            flops = sum(6.0 * H * W * T * K for H, W in shapes)
-            print(json.dumps({"workload": "ragged", "K": K, "step": step, "T": T, "ms": round(ms, 4),
-                              "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}), flush=True)
+            ms = statistics.median(times)
+            flops = step_flops(shapes, T, K)
+            cpu, _ = cpu_baseline(lambda i: cpu_oracle_step(256, 3000, T, K, seed=80 + i, rank=8),
+                                  cpu_s / 2, f"fused step of a 256x3000 row band (T={T}, K={K})")
+            out.append({"workload": f"ragged: 1000x3000, 5120x13824, 2048x50257 bf16, step {step} of the "
+                                    f"T schedule 64->128->256, T={T}, K={K}, fused step",
+                        "T": T, "K": K, "step": step, "ms_per_step": round(ms, 4),
+                        "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                        "l2": f"inputs larger than L2 ({nparams * 14 / 1e9:.2f} GB per step)",
+                        "roofline": roofline(flops, nparams * STEP_BYTES_PER_PARAM, ms * 1e-3, peaks,
+                                             peak_src),
+                        "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
+                        "cpu_baseline": cpu})
+            del Wc, Mc, Gs
+        del Ws, Ms
+    torch.cuda.empty_cache()
     assert hm.device_error(handle=handle) == 0
+    return out
+
+
+# ---------------------------------------------------------------- reference arm: the oracle
+
+def run_reference(args):
+    rank, world = env_int("RANK", 0), env_int("WORLD_SIZE", 1)
+    if rank != 0:
+        return
+    shapes, grank, T, K, chunk = workload_shapes(args.workload)
+    flops = step_flops(shapes, T, K)
+    nparams = sum(H * W for H, W in shapes)
+    H, W = CPU_SAMPLE_SHAPE
+    # each step: the oracle's fused step on the bounded sample (the same sample
+    # as the GPU arm's cpu_baseline); warm-up steps untimed
+    for i in range(args.warmup):
+        headline_cpu_sample(i, T, K)
+    secs, done = [], 0.0
+    for i in range(args.steps):
+        s, f = headline_cpu_sample(i, T, K)
+        secs.append(s)
+        done += f
+    rate = done / sum(secs)
+    value = rate / 1e12
+    sample = (f"per step: fused step of one {H}x{W} matrix ({H * W // (T * T)} tiles of T={T}, "
+              f"K={K}) in fp64; {args.steps} steps, {sum(secs):.1f} s")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(secs) * 1e3, 1),
+        "ms_per_step_measures": f"the bounded sample ({H}x{W}, one of the workload's 224 matrices)",
+        "ms_per_step_extrapolated_full_workload": round(flops / rate * 1e3, 1),
+        "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded low-rank + noise gradients)",
+        "config": {"workload": f"{args.workload}: {len(shapes)} matrices, {nparams / 1e9:.2f} G params, "
+                               f"T={T}, K={K}, fused momentum(0.95, Nesterov) + update(lr 0.02)",
+                   "T": T, "K": K, "matrices": len(shapes), "params": nparams,
+                   "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- stand-alone sweeps
+
+def run_sweep(args):
+    """Tile-size sweep on one 4096 x 4096 bf16 matrix alone (the same entries
+    as in ``secondary``), one JSON line per T."""
+    import torch
+
+    import tiled_newton_schulz_03_b300 as hm
+    from tiled_newton_schulz_03_b300 import build as hbuild
+    hbuild.build()
+    dev = torch.device("cuda", 0)
+    handle = hm.Handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, src = load_peaks()
+    args.secondary_cpu_seconds = 0.0
+    for e in run_secondary(hm, handle, dev, stream, peaks, src, args):
+        if e["workload"].startswith(args.workload):
+            print(json.dumps(e), flush=True)
     handle.close()
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["sweep4096", "ragged"],
                     default="llama3_8b",
                     help="llama3_8b (headline) or gpt2_small: the fused step, one JSON line; "
-                         "sweep4096 / ragged: secondary per-configuration timings")
+                         "sweep4096 / ragged: the secondary entries alone, one line each")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="skip the secondary workloads after the headline")
+    ap.add_argument("--secondary-reps", type=int, default=10)
+    ap.add_argument("--secondary-cpu-seconds", type=float, default=2.0)
     args = ap.parse_args()
-    if args.workload == "sweep4096" and args.impl == "ours":
+
+    world = env_int("WORLD_SIZE", 0)
+    if args.gpus > 1 and world == 0:
+        # not under torchrun: start one rank per GPU and pass the exit code on
+        cmd = relaunch_command(sys.argv[1:], args.gpus, _free_port())
+        sys.exit(subprocess.call(cmd))
+    if world and args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; running WORLD_SIZE ranks",
+              file=sys.stderr)
+
+    if args.workload in ("sweep4096", "ragged") and args.impl == "ours":
         run_sweep(args)
-    elif args.workload == "ragged" and args.impl == "ours":
-        run_ragged(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
