@@ -513,19 +513,28 @@ def _timed(fn, reps, stream, flush=None):
     return times
 
 
-def run_secondary(hm, handle, dev, stream, peaks, peak_src, args):
+def run_secondary(hm, handle, dev, stream, peaks, peak_src, args,
+                  groups=("gpt2_small", "sweep4096", "ragged")):
     """Configs measured besides the headline: the GPT-2-small fused step, the
     4096 x 4096 tile-size sweep (tiled NS only) and the ragged set with the
     runtime tile schedule. Each entry carries its roofline, the clocks seen
     while it ran, its kernel launches and an oracle CPU baseline on a sample."""
     import torch
+    out = []
+    fns = {"gpt2_small": _sec_gpt2, "sweep4096": _sec_sweep, "ragged": _sec_ragged}
+    for g in groups:
+        out += fns[g](hm, handle, dev, stream, peaks, peak_src, args)
+        torch.cuda.empty_cache()
+    assert hm.device_error(handle=handle) == 0
+    return out
+
+
+def _sec_gpt2(hm, handle, dev, stream, peaks, peak_src, args):
+    """GPT-2-small set, fused step, T = 128, K = 5."""
+    import torch
 
     from tiled_newton_schulz_03_b300 import synth
-    out = []
-    reps = max(5, args.secondary_reps)
-    cpu_s = args.secondary_cpu_seconds
-
-    # ---- GPT-2-small set, fused step, T = 128, K = 5
+    reps, cpu_s = max(5, args.secondary_reps), args.secondary_cpu_seconds
     shapes = synth.gpt2_small_shapes()
     Ws = [synth.gaussian(H, W, seed=10 + i, std=0.02, dtype=torch.bfloat16, device=dev) for i, (H, W) in enumerate(shapes)]
     Gs = [synth.lowrank_noise(H, W, seed=1 + 100 * i, rank=8, device=dev) for i, (H, W) in enumerate(shapes)]
@@ -542,16 +551,22 @@ def run_secondary(hm, handle, dev, stream, peaks, peak_src, args):
     flops = step_flops(shapes, 128, 5)
     cpu, _ = cpu_baseline(lambda i: cpu_oracle_step(768, 768, 128, 5, seed=40 + i, rank=8), cpu_s,
                           "fused step of one 768x768 matrix (36 tiles of T=128, K=5)")
-    out.append({"workload": f"gpt2_small: {len(shapes)} matrices, {nparams / 1e6:.1f} M params, "
-                            "T=128, K=5, fused momentum(0.95, Nesterov) + update(lr 0.02)",
-                "ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2),
-                "unit": UNIT, "l2": f"inputs larger than L2 ({nparams * 14 / 1e9:.2f} GB per step)",
-                "roofline": roofline(flops, nparams * STEP_BYTES_PER_PARAM, ms * 1e-3, peaks, peak_src),
-                "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
-                "cpu_baseline": cpu})
-    del Ws, Gs, Ms
+    return [{"workload": f"gpt2_small: {len(shapes)} matrices, {nparams / 1e6:.1f} M params, "
+                         "T=128, K=5, fused momentum(0.95, Nesterov) + update(lr 0.02)",
+             "ms_per_step": round(ms, 4), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+             "unit": UNIT, "l2": f"inputs larger than L2 ({nparams * 14 / 1e9:.2f} GB per step)",
+             "roofline": roofline(flops, nparams * STEP_BYTES_PER_PARAM, ms * 1e-3, peaks, peak_src),
+             "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
+             "cpu_baseline": cpu}]
 
-    # ---- 4096 x 4096 sweep, tiled NS only (bf16 in and out), K = 5
+
+def _sec_sweep(hm, handle, dev, stream, peaks, peak_src, args):
+    """4096 x 4096 sweep, tiled NS only (bf16 in and out), K = 5."""
+    import torch
+
+    from tiled_newton_schulz_03_b300 import synth
+    reps, cpu_s = max(5, args.secondary_reps), args.secondary_cpu_seconds
+    out = []
     G = synth.lowrank_noise(4096, 4096, seed=3, rank=8, device=dev)
     o = torch.empty_like(G)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)   # 256 MB > L2
@@ -576,9 +591,16 @@ def run_secondary(hm, handle, dev, stream, peaks, peak_src, args):
                     "roofline": roofline(flops, 4.0 * 4096 * 4096, ms * 1e-3, peaks, peak_src),
                     "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
                     "cpu_baseline": cpu})
-    del G, o, flush
+    return out
 
-    # ---- ragged set, three fused steps with T = 64 -> 128 -> 256, K = 3 and 5
+
+def _sec_ragged(hm, handle, dev, stream, peaks, peak_src, args):
+    """Ragged set, three fused steps with T = 64 -> 128 -> 256, K = 3 and 5."""
+    import torch
+
+    from tiled_newton_schulz_03_b300 import synth
+    reps, cpu_s = max(5, args.secondary_reps), args.secondary_cpu_seconds
+    out = []
     shapes = [(1000, 3000), (5120, 13824), (2048, 50257)]
     nparams = sum(H * W for H, W in shapes)
     sched = hm.TSchedule([(0, 64), (1, 128), (2, 256)])
@@ -614,8 +636,6 @@ def run_secondary(hm, handle, dev, stream, peaks, peak_src, args):
                         "cpu_baseline": cpu})
             del Wc, Mc, Gs
         del Ws, Ms
-    torch.cuda.empty_cache()
-    assert hm.device_error(handle=handle) == 0
     return out
 
 
@@ -667,8 +687,9 @@ def run_reference(args):
 # ---------------------------------------------------------------- stand-alone sweeps
 
 def run_sweep(args):
-    """Tile-size sweep on one 4096 x 4096 bf16 matrix alone (the same entries
-    as in ``secondary``), one JSON line per T."""
+    """One secondary workload alone (``--workload sweep4096`` or ``ragged``):
+    the same entries as in the headline line's ``secondary``, one JSON line
+    each."""
     import torch
 
     import tiled_newton_schulz_03_b300 as hm
@@ -679,9 +700,8 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     peaks, src = load_peaks()
     args.secondary_cpu_seconds = 0.0
-    for e in run_secondary(hm, handle, dev, stream, peaks, src, args):
-        if e["workload"].startswith(args.workload):
-            print(json.dumps(e), flush=True)
+    for e in run_secondary(hm, handle, dev, stream, peaks, src, args, groups=(args.workload,)):
+        print(json.dumps(e), flush=True)
     handle.close()
 
 

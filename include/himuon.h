@@ -18,9 +18,10 @@
  *     X <- X * s           s = 1 / (||X||_F + eps)      (norm = TILE, default)
  *                          s = 1 / (||G||_F + eps)      (norm = MATRIX)
  *                          s = 1                        (norm = NONE)
- *     repeat K times:  A = X X^T;  B = b A + c A^2;  X <- a X + B X
+ *     for k = 0 .. K-1:  A = X X^T;  B = b_k A + c_k A^2;  X <- a_k X + B X
  *     write X back at the tile's place.
- *   Defaults: (a, b, c) = (3.4445, -4.7750, 2.0315), eps = 1e-7.
+ *   Defaults: (a_k, b_k, c_k) = (3.4445, -4.7750, 2.0315) for every k,
+ *   eps = 1e-7.
  *
  * Conventions shared by every call below:
  *  - Matrices are row-major with a leading dimension (elements between the
@@ -77,12 +78,27 @@ typedef enum {
   HIMUON_PATH_FP32 = 2     /* fp32 validation path (CUDA cores, fp32 FMA) */
 } himuon_path;
 
-/* Parameters of the NS map. Fill with himuon_default_ns_params() first. */
+/*
+ * Parameters of the NS map. Fill with himuon_default_ns_params() first.
+ *
+ * Coefficients: by default every one of the K steps uses (a, b, c). A per-step
+ * schedule (step_coeffs != NULL) gives step k its own (a_k, b_k, c_k): the
+ * finite NS map is then the composition p_K o ... o p_1 of the odd polynomials
+ * p_k(s) = a_k s + b_k s^3 + c_k s^5 on the singular values. A step with
+ * c_k = 0 is a cubic step (two products instead of three), e.g. the classical
+ * polar iteration (1.5, -0.5, 0). The abstract fixes neither the coefficients
+ * nor that they are constant; both readings are parameters here.
+ */
 typedef struct {
-  float a, b, c;   /* NS coefficients, the same for all K steps */
+  float a, b, c;   /* NS coefficients of every step when step_coeffs is NULL */
   int32_t norm;    /* himuon_norm */
   float eps;       /* added to the Frobenius norm before dividing */
   int32_t path;    /* himuon_path */
+  const float* step_coeffs;  /* NULL, or HOST memory with 3 * K floats
+                                a_0, b_0, c_0, a_1, b_1, c_1, ...: the
+                                coefficients of step k = 0 .. K-1 (read during
+                                the call only; a, b, c are then ignored).
+                                Non-finite values: HIMUON_ERR_INVALID_ARG. */
 } himuon_ns_params;
 
 /* One matrix of a cross-layer batch (himuon_tiled_ns_batched). */
@@ -117,7 +133,8 @@ typedef struct himuon_handle himuon_handle;
 himuon_status himuon_create(himuon_handle** out_handle);
 himuon_status himuon_destroy(himuon_handle* handle);
 
-/* (a, b, c) = (3.4445, -4.7750, 2.0315), NORM_TILE, eps = 1e-7, PATH_AUTO. */
+/* (a, b, c) = (3.4445, -4.7750, 2.0315), NORM_TILE, eps = 1e-7, PATH_AUTO,
+   step_coeffs = NULL. */
 void himuon_default_ns_params(himuon_ns_params* p);
 
 /*

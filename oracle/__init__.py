@@ -17,6 +17,7 @@ from .himuon_oracle import (  # noqa: F401
     ns_steps,
     num_tiles,
     quintic_scalar,
+    step_coefficients,
     tile_grid,
     tiled_ns,
     tiled_ns_tiles,

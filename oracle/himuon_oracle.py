@@ -22,7 +22,9 @@ What the abstract leaves open, and the reading taken here (each one is also a
 parameter):
 
 * NS step: A = X X^T, B = b A + c A^2, X <- a X + B X, repeated K times, with the
-  quintic coefficients (a, b, c) = (3.4445, -4.7750, 2.0315) as default.
+  quintic coefficients (a, b, c) = (3.4445, -4.7750, 2.0315) as default. The
+  coefficients may also change from step to step (a per-step schedule of K
+  triples); a triple with c = 0 is a cubic step.
 * Normalisation before the first step: X <- X / (||X||_F + eps), eps = 1e-7, per
   tile by default ("tile"); "matrix" uses the norm of the whole matrix for every
   tile of it; "none" skips it.
@@ -76,15 +78,29 @@ def frobenius_normalise(X: np.ndarray, eps: float) -> np.ndarray:
     return X / (n + eps)
 
 
+def step_coefficients(coeffs, K: int):
+    """The (a, b, c) of each of the K steps.
+
+    ``coeffs`` is one triple (the same map at every step) or a sequence of K
+    triples (a per-step schedule: step k uses the k-th triple).
+    """
+    items = list(coeffs)
+    if len(items) == 3 and all(np.ndim(v) == 0 for v in items):
+        return [tuple(float(v) for v in items)] * K
+    if len(items) != K or any(len(t) != 3 for t in items):
+        raise ValueError(f"coeffs: one (a, b, c) triple or exactly K = {K} triples")
+    return [tuple(float(v) for v in t) for t in items]
+
+
 def ns_steps(X: np.ndarray, K: int, coeffs=QUINTIC) -> np.ndarray:
     """K steps of the finite NS map on an already normalised X.
 
-    Each step forms the Gram matrix A = X X^T, the polynomial B = b A + c A^2 and
-    the new iterate a X + B X. Works on one matrix (h, w) or a stack (n, h, w).
+    Step k forms the Gram matrix A = X X^T, the polynomial B = b_k A + c_k A^2
+    and the new iterate a_k X + B X, with (a_k, b_k, c_k) from
+    ``step_coefficients``. Works on one matrix (h, w) or a stack (n, h, w).
     """
-    a, b, c = (float(v) for v in coeffs)
     X = np.asarray(X, dtype=np.float64)
-    for _ in range(K):
+    for a, b, c in step_coefficients(coeffs, K):
         A = X @ np.swapaxes(X, -1, -2)
         B = b * A + c * (A @ A)
         X = a * X + B @ X
@@ -232,9 +248,9 @@ def full_mac_count(H: int, W: int, K: int) -> int:
 
 
 def quintic_scalar(sigma: float, K: int, coeffs=QUINTIC) -> float:
-    """The scalar polynomial p(x) = a x + b x^3 + c x^5 applied K times."""
-    a, b, c = coeffs
+    """The scalar polynomials p_k(x) = a_k x + b_k x^3 + c_k x^5, k = 0..K-1,
+    applied in turn."""
     x = float(sigma)
-    for _ in range(K):
+    for a, b, c in step_coefficients(coeffs, K):
         x = a * x + b * x ** 3 + c * x ** 5
     return x

@@ -362,3 +362,67 @@ def test_step_ns_input_with_tile_norm_is_direction_of_u():
     n = np.linalg.norm(u)
     # a rank-1 row: the NS step acts on its one singular value 1 after normalising
     np.testing.assert_allclose(O[0], u / n * float(_p1(Fraction(1))), rtol=1e-12, atol=0)
+
+
+# -- per-step coefficient schedules --------------------------------------------
+# Step k applies p_k(s) = a_k s + b_k s^3 + c_k s^5 to the singular values, so K
+# steps are the composition p_{K-1} o ... o p_0 (first triple first).
+
+MIXED = [(3.4445, -4.7750, 2.0315), (2.0, -1.5, 0.5), (1.5, -0.5, 0.0), (1.875, -1.25, 0.375)]
+
+
+def p_sched(x: Fraction, sched) -> Fraction:
+    for a, b, c in sched:
+        a, b, c = Fraction(a), Fraction(b), Fraction(c)
+        x = a * x + b * x ** 3 + c * x ** 5
+    return x
+
+
+@pytest.mark.parametrize("h,w", [(1, 1), (3, 5), (6, 4), (8, 8)])
+def test_schedule_matches_svd_closed_form(h, w):
+    X = rng(200 + 10 * h + w).standard_normal((h, w))
+    got = oracle.ns_map(X, len(MIXED), MIXED, "tile", 1e-7)
+    U, S, Vt = np.linalg.svd(X, full_matrices=False)
+    s = S / (np.linalg.norm(S) + 1e-7)
+    f = np.array([float(p_sched(Fraction(float(v)), MIXED)) for v in s])
+    np.testing.assert_allclose(got, (U * f) @ Vt, rtol=0, atol=1e-11)
+
+
+def test_schedule_order_is_first_triple_first():
+    X = rng(31).standard_normal((5, 7))
+    fwd = oracle.ns_map(X, 4, MIXED, "tile", 0.0)
+    rev = oracle.ns_map(X, 4, MIXED[::-1], "tile", 0.0)
+    assert np.max(np.abs(fwd - rev)) > 1e-3
+    # 1 x 1 hand value: x = 1 after normalisation; p_0(1) = a+b+c = 0.701,
+    # then the cubic 2 - 1.5 + 0.5 at 0.701, ...
+    x = oracle.ns_map(np.array([[3.0]]), 2, MIXED[:2], "tile", 0.0)[0, 0]
+    y = Fraction(7010, 10000)
+    want = 2 * y - Fraction(3, 2) * y ** 3 + Fraction(1, 2) * y ** 5
+    assert abs(x - float(want)) < 1e-13
+
+
+def test_constant_schedule_equals_single_triple_exactly():
+    G = rng(32).standard_normal((20, 13))
+    one = oracle.tiled_ns(G, 8, 5, QUINTIC)
+    many = oracle.tiled_ns(G, 8, 5, [QUINTIC] * 5)
+    assert np.array_equal(one, many)
+
+
+def test_quintic_then_cubic_schedule_reaches_polar_factor():
+    # the quintic leaves singular values in a band around 1; cubic Newton-Schulz
+    # steps (Bjorck-Bowie) then converge them to exactly 1: the polar factor
+    r = rng(33)
+    U, _ = np.linalg.qr(r.standard_normal((9, 6)))
+    V, _ = np.linalg.qr(r.standard_normal((6, 6)))
+    X = U @ np.diag(np.geomspace(1.0, 0.05, 6)) @ V.T
+    sched = [QUINTIC] * 5 + [(1.5, -0.5, 0.0)] * 25
+    out = oracle.ns_map(X, len(sched), sched, "tile", 1e-7)
+    np.testing.assert_allclose(out, U @ V.T, rtol=0, atol=1e-10)
+    # the quintic alone does not: its fixed band is not {1}
+    q = oracle.ns_map(X, 30, QUINTIC, "tile", 1e-7)
+    assert np.max(np.abs(q - U @ V.T)) > 1e-2
+
+
+def test_schedule_length_must_be_K():
+    with pytest.raises(ValueError):
+        oracle.ns_map(np.eye(3), 3, MIXED, "tile", 0.0)

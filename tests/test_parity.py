@@ -97,6 +97,57 @@ def test_other_coefficients(T):
     assert rel_fro(f64(out), want) <= TOL_BF16
 
 
+# ---------------------------------------------------------------- per-step coefficient schedules
+
+# three quintic steps, a quintic with p(1) = 1 and p'(1) = 0, then a cubic
+# (c = 0: two products instead of three) polishing step
+SCHED = [(3.4445, -4.7750, 2.0315)] * 3 + [(2.0, -1.5, 0.5), (1.5, -0.5, 0.0)]
+
+
+@pytest.mark.parametrize("T,path", [(32, "tensor"), (64, "tensor"), (128, "tensor"), (256, "tensor"),
+                                    (100, "tensor"), (1024, "tensor"), (16, "tensor"),
+                                    (128, "fp32"), (64, "fp32")])
+def test_per_step_schedule_matches_oracle(T, path):
+    G = synth.lowrank_noise(300, 530, seed=T + 7)
+    out = hm.tiled_ns(G.cuda(), T, 5, coeffs=SCHED, path=path, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5, SCHED)
+    assert rel_fro(f64(out), want) <= (TOL_BF16 if path == "tensor" else TOL_FP32)
+    # a wrong step order would give another map: the check can tell them apart
+    assert rel_fro(oracle.tiled_ns(f64(G), T, 5, SCHED[::-1]), want) > 4 * TOL_BF16
+
+
+@pytest.mark.parametrize("T", [32, 64, 128, 256])
+def test_constant_schedule_equals_single_triple_bit_exact(T):
+    G = synth.lowrank_noise(384, 520, seed=T).cuda()
+    one = hm.tiled_ns(G, T, 5, path="tensor")
+    many = hm.tiled_ns(G, T, 5, coeffs=[hm.QUINTIC] * 5, path="tensor")
+    assert torch.equal(one, many)
+
+
+@pytest.mark.parametrize("T", [128, 64, 32])
+def test_step_with_schedule_matches_oracle(T):
+    shapes = [(768, 768), (300, 530)]
+    Ws, Gs, Ms = _step_case(shapes, 120)
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95, coeffs=SCHED, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], T, 5, lr=0.02, mu=0.95,
+                                       coeffs=SCHED)
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16)
+
+
+def test_schedule_errors():
+    G = synth.lowrank_noise(64, 64, seed=1).cuda()
+    with pytest.raises(hm.HimuonError):                   # K triples needed
+        hm.tiled_ns(G, 64, 5, coeffs=SCHED[:4])
+    bad = list(SCHED)
+    bad[2] = (float("nan"), 0.0, 0.0)
+    with pytest.raises(hm.HimuonError) as e:              # checked on the host, nothing launched
+        hm.tiled_ns(G, 64, 5, coeffs=bad)
+    assert e.value.status_name == "INVALID_ARG" and "step 2" in str(e.value)
+
+
 # ---------------------------------------------------------------- bit-exact structure
 
 @pytest.mark.parametrize("T", [128, 64, 32, 256])   # on-chip (two), warp-tile and GEMM kernels
@@ -235,6 +286,29 @@ def test_step_matches_oracle(path, wdtype):
         check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16 if path == "tensor" else TOL_FP32)
 
 
+@pytest.mark.parametrize("T,H,W", [(128, 384, 256), (128, 256, 520), (64, 320, 200), (64, 192, 448)])
+def test_step_weight_reduce_add_is_one_rounding_of_w_plus_update(T, H, W):
+    """bf16 weights with 16-byte aligned rows and no weight decay take their
+    update by a TMA reduce-add of D = bf16(-lr s O) onto W. From W0 = 0 the step
+    stores D itself; from any W0 (same G and M) it must store bf16_rne(W0 + D),
+    element for element. Shapes with aligned rows and tall or full tiles only
+    (unaligned rows and wide edge tiles take the read-modify-write, one rounding
+    of W0 + fp32 update); right-edge tiles narrower than a 64-column box (8 and
+    8 columns at 520 and 200) check the box clipping."""
+    G = synth.lowrank_noise(H, W, seed=T + H).cuda()
+    M0 = synth.gaussian(H, W, 3, std=1e-3).cuda()
+    W0 = synth.gaussian(H, W, 4, std=0.02, dtype=torch.bfloat16).cuda()
+    Wz, Mz = torch.zeros_like(W0), M0.clone()
+    hm.step([Wz], [G], [Mz], T, 5, lr=0.02, mu=0.95, path="tensor")
+    Wa, Ma = W0.clone(), M0.clone()
+    hm.step([Wa], [G], [Ma], T, 5, lr=0.02, mu=0.95, path="tensor")
+    assert torch.equal(Ma, Mz)
+    want = (W0.float() + Wz.float()).to(torch.bfloat16)
+    assert torch.equal(Wa, want)
+    Wn, _, _ = oracle.himuon_step(np.zeros((H, W)), f64(G), f64(M0), T, 5, lr=0.02, mu=0.95)
+    check_update(f64(Wz), np.zeros((H, W)), Wn, TOL_BF16)
+
+
 def test_step_zero_lr_keeps_weights_and_updates_momentum():
     Ws, Gs, Ms = _step_case([(256, 384)], 60)
     W0 = Ws[0].clone()
@@ -317,7 +391,54 @@ def test_step_weight_decay_and_fp32_weights():
     check_update(f64(Ws[0]), W0, Wn, TOL_BF16)
 
 
-# ---------------------------------------------------------------- large tiles and full matrix (GEMM path)
+# ---------------------------------------------------------------- 128 < T <= 256: one tile on a pair of SMs
+
+@pytest.mark.parametrize("T,H,W", [(256, 300, 530), (256, 1000, 300), (256, 512, 512), (200, 450, 700),
+                                   (160, 330, 170), (129, 260, 390), (256, 44, 600), (256, 600, 81)])
+def test_pair_kernel_matches_oracle(T, H, W):
+    """Tiles zero-padded to 256 x 256, held on two SMs. Wide edge tiles (fewer
+    rows than columns, e.g. 44 x 256) run transposed, tall ones (600 x 81) as
+    they are; T = 129 and 200 give tile origins that are not 16-byte aligned."""
+    G = synth.lowrank_noise(H, W, seed=H + 3 * W + T)
+    out = hm.tiled_ns(G.cuda(), T, 5, path="tensor", out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_pair_kernel_small_K_and_fp32_input(K):
+    G = synth.gaussian(384, 520, seed=K)                  # fp32 input
+    out = hm.tiled_ns(G.cuda(), 256, K, path="tensor", out_dtype=torch.float32)
+    assert rel_fro(f64(out), oracle.tiled_ns(f64(G), 256, K)) <= TOL_BF16
+    o16 = hm.tiled_ns(G.cuda(), 256, K, path="tensor", out_dtype=torch.bfloat16)
+    assert torch.equal(o16, out.to(torch.bfloat16))      # one rounding of the same fp32 result
+
+
+@pytest.mark.parametrize("T", [256, 200])
+def test_pair_kernel_step_matches_oracle(T):
+    shapes = [(768, 768), (300, 530), (1000, 300), (520, 1030)]
+    Ws, Gs, Ms = _step_case(shapes, 130 + T)
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95, nesterov=True, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], T, 5, lr=0.02, mu=0.95)
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16)
+
+
+def test_pair_kernel_step_weight_decay_fp32_weights_bf16_momentum():
+    shapes = [(512, 300), (260, 700)]
+    Ws, Gs, Ms = _step_case(shapes, 140, mdtype=torch.bfloat16, wdtype=torch.float32)
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, 256, 5, lr=0.01, mu=0.9, weight_decay=0.05, nesterov=False, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 256, 5, lr=0.01, mu=0.9,
+                                       weight_decay=0.05, nesterov=False)
+        assert rel_fro(f64(Ms[i]), Mn) <= 2.0 ** -8       # bf16 momentum buffer: unit roundoff
+        check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16)
+
+
+# ---------------------------------------------------------------- other large tiles and the full matrix
 
 @pytest.mark.parametrize("H,W,T", [(300, 530, 256), (1000, 300, 256), (513, 200, 384),
                                    (600, 640, 4096), (1024, 1024, 1024), (130, 700, 96),

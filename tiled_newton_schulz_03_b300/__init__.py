@@ -62,7 +62,8 @@ class HimuonError(RuntimeError):
 
 class NSParams(ctypes.Structure):
     _fields_ = [("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
-                ("norm", ctypes.c_int32), ("eps", ctypes.c_float), ("path", ctypes.c_int32)]
+                ("norm", ctypes.c_int32), ("eps", ctypes.c_float), ("path", ctypes.c_int32),
+                ("step_coeffs", ctypes.POINTER(ctypes.c_float))]
 
 
 class Matrix(ctypes.Structure):
@@ -199,13 +200,33 @@ def _mat_info(t: torch.Tensor, name: str):
     return t.data_ptr(), t.size(0), t.size(1), ld, _DTYPE[t.dtype]
 
 
-def _ns_params(coeffs, norm, eps, path) -> NSParams:
-    a, b, c = (float(v) for v in coeffs)
+def _step_schedule(coeffs, K: int):
+    """None for one (a, b, c) triple used at every step; else the flat list of
+    K per-step triples (a_k, b_k, c_k)."""
+    items = list(coeffs)
+    if len(items) == 3 and all(not isinstance(v, (list, tuple)) for v in items):
+        return None
+    if len(items) != K or any(len(t) != 3 for t in items):
+        raise HimuonError(1, f"coeffs: one (a, b, c) triple, or exactly K = {K} triples")
+    return [float(v) for t in items for v in t]
+
+
+def _ns_params(coeffs, norm, eps, path, K: int) -> NSParams:
+    """ctypes parameters of the NS map. ``coeffs`` is one (a, b, c) triple for
+    every step, or a list of K triples (a per-step schedule)."""
     if norm not in _NORM:
         raise HimuonError(1, f"unknown norm mode {norm!r}")
     if path not in _PATH:
         raise HimuonError(1, f"unknown path {path!r}")
-    return NSParams(a, b, c, _NORM[norm], float(eps), _PATH[path])
+    sched = _step_schedule(coeffs, int(K))
+    if sched is None:
+        a, b, c = (float(v) for v in coeffs)
+        return NSParams(a, b, c, _NORM[norm], float(eps), _PATH[path], None)
+    arr = (ctypes.c_float * len(sched))(*sched)
+    p = NSParams(sched[0], sched[1], sched[2], _NORM[norm], float(eps), _PATH[path],
+                 ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)))
+    p._keep = arr                      # the array lives as long as the parameters
+    return p
 
 
 def tiled_ns(G: torch.Tensor, T: int, K: int = 5, coeffs=QUINTIC, norm: str = "tile",
@@ -219,7 +240,7 @@ def tiled_ns(G: torch.Tensor, T: int, K: int = 5, coeffs=QUINTIC, norm: str = "t
     if (H2, W2) != (H, W):
         raise HimuonError(1, "out must have the shape of G")
     h = handle or _default_handle(G.device)
-    p = _ns_params(coeffs, norm, eps, path)
+    p = _ns_params(coeffs, norm, eps, path, K)
     with torch.cuda.device(G.device):
         _check(load_library().himuon_tiled_ns(h.ptr, g, H, W, ldg, gt, int(T), int(K),
                                               ctypes.byref(p), o, ldo, ot,
@@ -243,7 +264,7 @@ def tiled_ns_fp32_noalloc(G: torch.Tensor, T: int, K: int = 5, coeffs=QUINTIC,
     o, H2, W2, ldo, ot = _mat_info(out, "out")
     if (H2, W2) != (H, W):
         raise HimuonError(1, "out must have the shape of G")
-    p = _ns_params(coeffs, norm, eps, "fp32")
+    p = _ns_params(coeffs, norm, eps, "fp32", K)
     with torch.cuda.device(G.device):
         _check(load_library().himuon_tiled_ns_fp32_noalloc(g, H, W, ldg, gt, int(T), int(K),
                                                            ctypes.byref(p), o, ldo, ot,
@@ -273,7 +294,7 @@ def tiled_ns_batched(Gs, T: int, K: int = 5, coeffs=QUINTIC, norm: str = "tile",
             raise HimuonError(1, "all matrices must be on one device")
         arr[i] = Matrix(g, o, H, W, ldg, ldo, gt, ot)
     h = handle or _default_handle(Gs[0].device)
-    p = _ns_params(coeffs, norm, eps, path)
+    p = _ns_params(coeffs, norm, eps, path, K)
     with torch.cuda.device(Gs[0].device):
         _check(load_library().himuon_tiled_ns_batched(h.ptr, arr, len(Gs), int(T), int(K),
                                                       ctypes.byref(p), int(chunk_bytes),
@@ -300,7 +321,7 @@ def step(Ws, Gs, Ms, T: int, K: int = 5, lr: float = 0.02, mu: float = 0.95,
             raise HimuonError(1, f"shapes of Ws[{i}], Gs[{i}], Ms[{i}] differ")
         arr[i] = Param(w, g, m, H, W, ldw, ldg, ldm, wt, gt, mt)
     h = handle or _default_handle(Ws[0].device)
-    p = _ns_params(coeffs, norm, eps, path)
+    p = _ns_params(coeffs, norm, eps, path, K)
     sp = StepParams(float(lr), float(mu), float(weight_decay), 1 if nesterov else 0, _SCALE[scale_mode])
     with torch.cuda.device(Ws[0].device):
         _check(load_library().himuon_step(h.ptr, arr, len(Ws), int(T), int(K), ctypes.byref(p),

@@ -37,7 +37,7 @@ himuon_status cuda_fail(cudaError_t e, const char* where) {
   return fail(HIMUON_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
 }
 
-constexpr int32_t kMaxK = 64;
+constexpr int32_t kMaxK = kMaxSteps;
 constexpr int64_t kMaxDim = (1LL << 31) - 1024;
 constexpr size_t kFp32ScratchCap = size_t(512) << 20;  // bytes of fp32-path scratch per sub-batch
 
@@ -69,10 +69,31 @@ himuon_status check_ns_params(const himuon_ns_params& p) {
     return fail(HIMUON_ERR_INVALID_ARG, "ns params: unknown norm mode");
   if (!(p.path == HIMUON_PATH_AUTO || p.path == HIMUON_PATH_TENSOR || p.path == HIMUON_PATH_FP32))
     return fail(HIMUON_ERR_INVALID_ARG, "ns params: unknown path");
-  if (!std::isfinite(p.a) || !std::isfinite(p.b) || !std::isfinite(p.c))
+  if (!p.step_coeffs && (!std::isfinite(p.a) || !std::isfinite(p.b) || !std::isfinite(p.c)))
     return fail(HIMUON_ERR_INVALID_ARG, "ns params: coefficients must be finite");
   if (!(p.eps >= 0.f) || !std::isfinite(p.eps))
     return fail(HIMUON_ERR_INVALID_ARG, "ns params: eps must be finite and >= 0");
+  return HIMUON_OK;
+}
+
+// Kernel arguments of the NS map: the coefficients of every step (the same
+// triple K times, or the caller's per-step schedule), normalisation, K and T.
+himuon_status make_ns_args(const himuon_ns_params& p, int32_t K, int32_t T, NSArgs* ns) {
+  std::memset(ns, 0, sizeof(NSArgs));
+  ns->eps = p.eps;
+  ns->norm = p.norm;
+  ns->K = K;
+  ns->T = T;
+  for (int32_t k = 0; k < K; ++k) {
+    const float* c = p.step_coeffs ? p.step_coeffs + 3 * k : nullptr;
+    ns->coef[k][0] = c ? c[0] : p.a;
+    ns->coef[k][1] = c ? c[1] : p.b;
+    ns->coef[k][2] = c ? c[2] : p.c;
+    if (!std::isfinite(ns->coef[k][0]) || !std::isfinite(ns->coef[k][1]) ||
+        !std::isfinite(ns->coef[k][2]))
+      return fail(HIMUON_ERR_INVALID_ARG,
+                  "ns params: coefficients of step " + std::to_string(k) + " must be finite");
+  }
   return HIMUON_OK;
 }
 
@@ -253,7 +274,9 @@ himuon_status run_gemm_path(himuon_handle* h, const std::vector<MatDesc>& descs,
                                  h->scratch, h->wait_ns, h->d_err, stream, &ms);
         if (ms != HIMUON_OK) return fail(ms, "GEMM path: tensor map encoding failed");
         if (e != cudaSuccess) return cuda_fail(e, "GEMM path launch");
-        h->launches += 2 + (ns.K == 0 ? 1 : ns.K * (ns.c != 0.f ? 3 : 2));
+        int64_t per_step = 0;
+        for (int k = 0; k < ns.K; ++k) per_step += step_coef(ns, k).has_c ? 3 : 2;
+        h->launches += 2 + (ns.K == 0 ? 1 : per_step);
       }
     }
   }
@@ -287,11 +310,13 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
 
   const bool fp32 = p.path == HIMUON_PATH_FP32;
   // tensor path: T <= 32 one tile per warp (ns_mma32.cu); T = 64 and 128 on
-  // chip (ns_tc.cu); T > 64 otherwise, and
-  // the full-matrix map, run as batched GEMMs (ns_gemm.cu)
-  // T <= 32: one warp per tile (ns_mma32.cu)
+  // one SM (ns_tc.cu); 128 < T <= 256 on a pair of SMs (ns_pair.cu); every
+  // other T > 64, and the full-matrix map, as batched GEMMs (ns_gemm.cu)
   const bool warp_tiles = T <= 32;
   const bool onchip = T == 64 || T == 128;
+  // 128 < T <= 256: one tile on a pair of SMs (ns_pair.cu); K = 0 has no
+  // products and takes the GEMM path's gather/emit kernels
+  const bool pair = T > 128 && T <= 256 && K > 0;
   if (!fp32 && !onchip && !warp_tiles && T < 64) {
     return fail(HIMUON_ERR_UNSUPPORTED,
                 "tensor path: T = " + std::to_string(T) +
@@ -300,17 +325,22 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
 
   // ---- TMA staging where the layouts allow it (16-byte aligned rows; for a
   // step bf16 G and fp32 M; T >= 64, since a 32-column box is narrower than the
-  // 128-byte staging rows); other matrices are staged with plain loads.
-  std::vector<CUtensorMap> maps((fp32 || !onchip) ? 0 : 2 * static_cast<size_t>(n));
+  // 128-byte staging rows); other matrices are staged with plain loads. For a
+  // step without weight decay, bf16 weights with 16-byte aligned rows are
+  // updated by a TMA reduce-add (W += -lr s O) instead of a read-modify-write.
+  std::vector<CUtensorMap> maps((fp32 || !onchip) ? 0 : 3 * static_cast<size_t>(n));
   for (int i = 0; i < n && !fp32 && onchip; ++i) {
     MatDesc& d = descs[i];
     const bool in32 = d.flags & F_IN_FP32;
     bool ok = (d.flags & F_IN_VEC) != 0 && T >= 64;
     if (st.enabled) ok = ok && !in32 && (d.flags & F_M_VEC) && !(d.flags & F_M_BF16);
-    std::memset(&maps[2 * i], 0, 2 * sizeof(CUtensorMap));
-    if (ok) ok = make_map(&maps[2 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
-    if (ok && st.enabled) ok = make_map(&maps[2 * i + 1], d.mom, d.H, d.W, d.ld_mom, true, 32, T);
+    std::memset(&maps[3 * i], 0, 3 * sizeof(CUtensorMap));
+    if (ok) ok = make_map(&maps[3 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
+    if (ok && st.enabled) ok = make_map(&maps[3 * i + 1], d.mom, d.H, d.W, d.ld_mom, true, 32, T);
     if (ok) d.flags |= F_TMA;
+    if (st.enabled && st.wd_factor == 1.f && !(d.flags & F_OUT_FP32) && (d.flags & F_OUT_VEC) &&
+        make_map(&maps[3 * i + 2], d.out, d.H, d.W, d.ld_out, false, 64, T))
+      d.flags |= F_W_TMA;
   }
 
   // ---- per-matrix norm partials
@@ -341,7 +371,8 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   const void* d_maps = ws + off_maps;
   float* d_partials = reinterpret_cast<float*>(ws + off_partials);
 
-  NSArgs ns{p.a, p.b, p.c, p.eps, p.norm, K, T};
+  NSArgs ns;
+  if ((s = make_ns_args(p, K, T, &ns)) != HIMUON_OK) return s;
   if (p.norm == HIMUON_NORM_MATRIX) {
     e = launch_matrix_norms(d_descs, n, d_part, nparts, d_partials, p.eps, st, stream);
     if (e != cudaSuccess) return cuda_fail(e, "matrix norm launch");
@@ -415,6 +446,15 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
     }
     return HIMUON_OK;
   }
+  if (pair) {
+    for (auto& c : chunks) {
+      e = launch_ns_pair(d_descs, n, c.first, c.second, ns, st, h->wait_ns, h->d_err, h->num_sms,
+                         stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor path launch");
+      h->launches += 1;
+    }
+    return HIMUON_OK;
+  }
   return run_gemm_path(h, descs, d_descs, T, ns, st, chunks, stream);
 }
 
@@ -473,6 +513,7 @@ void himuon_default_ns_params(himuon_ns_params* p) {
   p->norm = HIMUON_NORM_TILE;
   p->eps = 1e-7f;
   p->path = HIMUON_PATH_AUTO;
+  p->step_coeffs = nullptr;
 }
 
 double himuon_ns_flops(int64_t H, int64_t W, int32_t T, int32_t K) {
@@ -592,6 +633,10 @@ himuon_status himuon_tiled_ns_batched(himuon_handle* h, const himuon_matrix* mat
   if ((s = check_ns_params(p)) != HIMUON_OK) return s;
   if (T < 1) return fail(HIMUON_ERR_INVALID_ARG, "T must be >= 1");
   if (K < 0 || K > kMaxK) return fail(HIMUON_ERR_INVALID_ARG, "K must be in [0, 64]");
+  {
+    NSArgs probe;   // every step's coefficients checked before anything is enqueued
+    if ((s = make_ns_args(p, K, T, &probe)) != HIMUON_OK) return s;
+  }
   std::vector<MatDesc> descs(n);
   for (int32_t i = 0; i < n; ++i) {
     const himuon_matrix& m = mats[i];
@@ -638,6 +683,10 @@ himuon_status himuon_step(himuon_handle* h, const himuon_param* params, int32_t 
   if ((s = check_ns_params(p)) != HIMUON_OK) return s;
   if (T < 1) return fail(HIMUON_ERR_INVALID_ARG, "T must be >= 1");
   if (K < 0 || K > kMaxK) return fail(HIMUON_ERR_INVALID_ARG, "K must be in [0, 64]");
+  {
+    NSArgs probe;   // every step's coefficients checked before anything is enqueued
+    if ((s = make_ns_args(p, K, T, &probe)) != HIMUON_OK) return s;
+  }
   if (!std::isfinite(step->lr) || !std::isfinite(step->mu) || !std::isfinite(step->weight_decay))
     return fail(HIMUON_ERR_INVALID_ARG, "step params must be finite");
   if (!(step->scale_mode == 0 || step->scale_mode == 1))

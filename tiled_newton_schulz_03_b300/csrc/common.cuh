@@ -22,6 +22,7 @@ enum : int32_t {
   F_OUT_VEC = 1 << 4,     // 16-byte vector stores/loads of out / W are legal
   F_M_VEC = 1 << 5,       // 16-byte vector access of M is legal
   F_TMA = 1 << 6,         // tensor maps of G (and M for a step) exist: TMA staging
+  F_W_TMA = 1 << 7,       // step: W (bf16, no weight decay) is updated by a TMA reduce-add
 };
 
 struct MatDesc {
@@ -52,12 +53,34 @@ struct GTile {
 };
 static_assert(sizeof(GTile) == 32, "GTile layout");
 
+constexpr int kMaxSteps = 64;
+
+// NS parameters of a launch. coef[k] = (a_k, b_k, c_k) of step k, filled for
+// k < K: the same triple for every step, or a per-step schedule.
 struct NSArgs {
-  float a, b, c, eps;
+  float eps;
   int32_t norm;
   int32_t K;
   int32_t T;
+  float coef[kMaxSteps][3];
 };
+
+// Coefficients of one NS step, with the shift e = a - min(a, 1.5) that the
+// tensor-core kernels move from a X into the bf16 operand C = B + e I.
+struct StepCoef {
+  float a, b, c, e;
+  bool has_c;        // c != 0: the step needs the product A A
+};
+
+__host__ __device__ __forceinline__ StepCoef step_coef(const NSArgs& ns, int k) {
+  StepCoef s;
+  s.a = ns.coef[k][0];
+  s.b = ns.coef[k][1];
+  s.c = ns.coef[k][2];
+  s.e = s.a > 1.5f ? s.a - 1.5f : 0.f;
+  s.has_c = s.c != 0.f;
+  return s;
+}
 
 struct StepArgs {
   float mu;

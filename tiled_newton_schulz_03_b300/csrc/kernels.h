@@ -13,12 +13,21 @@
 namespace himuon {
 
 // Tensor-core tiled NS, T in {64, 128} (ns_tc.cu). descs: device array of ndesc
-// MatDesc; maps: device array of 2 * ndesc CUtensorMap (G, M), 64-byte aligned,
-// valid for matrices flagged F_TMA; tiles [tile_begin, tile_end) of the flat
-// tile list are processed. st.enabled selects the fused HiMuon step.
+// MatDesc; maps: device array of 3 * ndesc CUtensorMap (G, M, W), 64-byte
+// aligned; G and M valid for matrices flagged F_TMA, W for those flagged
+// F_W_TMA; tiles [tile_begin, tile_end) of the flat tile list are processed.
+// st.enabled selects the fused HiMuon step.
 cudaError_t launch_ns_tc(const MatDesc* descs, const void* maps, int ndesc, int64_t tile_begin,
                          int64_t tile_end, const NSArgs& ns, const StepArgs& st, uint64_t wait_ns,
                          int* err, int num_sms, cudaStream_t stream);
+
+// Tensor-core tiled NS for 128 < T <= 256, K >= 1 (ns_pair.cu): one tile per
+// cluster of two CTAs (cta_group::2 products), held on chip for all K steps;
+// plain global loads and stores (any alignment). Same arguments as
+// launch_ns_tc without the tensor maps.
+cudaError_t launch_ns_pair(const MatDesc* descs, int ndesc, int64_t tile_begin, int64_t tile_end,
+                           const NSArgs& ns, const StepArgs& st, uint64_t wait_ns, int* err,
+                           int num_sms, cudaStream_t stream);
 
 // Tensor-core tiled NS for T <= 32 (ns_mma32.cu): one warp per tile, warp-level
 // mma.sync; any alignment, plain loads. Same arguments as launch_ns_tc without

@@ -93,8 +93,8 @@ himuon_status himuon_tiled_ns_fp32_noalloc(const void* G, int64_t H, int64_t W, 
   if (params) p = *params;
   if (!(p.norm == HIMUON_NORM_TILE || p.norm == HIMUON_NORM_MATRIX || p.norm == HIMUON_NORM_NONE))
     return nfail(HIMUON_ERR_INVALID_ARG, "ns params: unknown norm mode");
-  if (!std::isfinite(p.a) || !std::isfinite(p.b) || !std::isfinite(p.c) || !std::isfinite(p.eps) ||
-      !(p.eps >= 0.f))
+  if ((!p.step_coeffs && (!std::isfinite(p.a) || !std::isfinite(p.b) || !std::isfinite(p.c))) ||
+      !std::isfinite(p.eps) || !(p.eps >= 0.f))
     return nfail(HIMUON_ERR_INVALID_ARG, "ns params: coefficients and eps must be finite, eps >= 0");
   if (!G || !out) return nfail(HIMUON_ERR_INVALID_ARG, "NULL pointer");
   if (!(gtype == HIMUON_BF16 || gtype == HIMUON_FP32) || !(otype == HIMUON_BF16 || otype == HIMUON_FP32))
@@ -112,6 +112,23 @@ himuon_status himuon_tiled_ns_fp32_noalloc(const void* G, int64_t H, int64_t W, 
       return nfail(HIMUON_ERR_INVALID_ARG, "output partially overlaps the input");
     if (G == out && (ldg != ldo || gtype != otype))
       return nfail(HIMUON_ERR_INVALID_ARG, "in-place needs the same ld and dtype");
+  }
+
+  // ---- coefficients of every step (checked before anything is enqueued)
+  NSArgs ns;
+  std::memset(&ns, 0, sizeof(ns));
+  ns.eps = p.eps;
+  ns.norm = p.norm;
+  ns.K = K;
+  ns.T = T;
+  for (int32_t k = 0; k < K; ++k) {
+    const float* c = p.step_coeffs ? p.step_coeffs + 3 * k : nullptr;
+    ns.coef[k][0] = c ? c[0] : p.a;
+    ns.coef[k][1] = c ? c[1] : p.b;
+    ns.coef[k][2] = c ? c[2] : p.c;
+    if (!std::isfinite(ns.coef[k][0]) || !std::isfinite(ns.coef[k][1]) || !std::isfinite(ns.coef[k][2]))
+      return nfail(HIMUON_ERR_INVALID_ARG, "ns params: coefficients of step " + std::to_string(k) +
+                                               " must be finite");
   }
 
   // ---- fit into the fixed scratch
@@ -176,7 +193,6 @@ himuon_status himuon_tiled_ns_fp32_noalloc(const void* G, int64_t H, int64_t W, 
   float* d_partials = reinterpret_cast<float*>(base + kOffPartials);
   float* d_tiles = reinterpret_cast<float*>(base + off_tiles);
 
-  NSArgs ns{p.a, p.b, p.c, p.eps, p.norm, K, T};
   StepArgs stp{0.f, 1.f, 0, 0};
   if (p.norm == HIMUON_NORM_MATRIX) {
     e = launch_matrix_norms(d_desc, 1, d_part, nparts, d_partials, p.eps, stp, st);

@@ -205,8 +205,9 @@ cudaError_t launch_ns_fp32(const MatDesc* descs, int ndesc, int64_t tile_begin, 
     const dim3 g((P + 63) / 64, (P + 63) / 64, n);
     for (int k = 0; k < ns.K; ++k) {
       f32_gemm<true><<<g, 256, 0, stream>>>(X, X, nullptr, A, P, 1.f, 0.f);
-      f32_gemm<false><<<g, 256, 0, stream>>>(A, A, A, B, P, ns.c, ns.b);
-      f32_gemm<false><<<g, 256, 0, stream>>>(B, X, X, A, P, 1.f, ns.a);
+      const StepCoef cf = step_coef(ns, k);
+      f32_gemm<false><<<g, 256, 0, stream>>>(A, A, A, B, P, cf.c, cf.b);
+      f32_gemm<false><<<g, 256, 0, stream>>>(B, X, X, A, P, 1.f, cf.a);
       std::swap(X, A);
     }
     f32_scatter<<<n, 256, 0, stream>>>(descs, ndesc, t0, T, P, X, st);

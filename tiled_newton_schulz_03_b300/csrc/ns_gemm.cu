@@ -237,7 +237,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
     const int r = m0 + 32 * q + lane;                  // oriented row within the tile
     const uint32_t taddr = tbase + (static_cast<uint32_t>(32 * q) << 16);
     const GTile& t = g.tiles[p];
-    const float e = g.ns.a > 1.5f ? g.ns.a - 1.5f : 0.f;
+    const StepCoef cf = step_coef(g.ns, g.step);       // this NS step's (a, b, c)
+    const float e = cf.e;
     const int64_t hh = static_cast<int64_t>(g.Hp) * g.Hp, hw = static_cast<int64_t>(g.Hp) * g.Wp;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
       ptx::tmem_ld32_sync(taddr + 32 * ch, v);
       if (MODE == G_GRAM) {
         const float s2 = g.step == 0 ? t.s * t.s : 1.f;
-        const bool has_c = g.ns.c != 0.f;
+        const bool has_c = cf.has_c;
         // A = s^2 R; with c = 0 there is no A A product: write C = b A + e I directly
         __nv_bfloat16* dst = (has_c ? g.ab : g.cb) + p * hh + static_cast<int64_t>(r) * g.Hp + c0;
         uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             float x = v[8 * qd + j] * s2;
-            if (!has_c) x = x * g.ns.b + ((c0 + 8 * qd + j == r) ? e : 0.f);
+            if (!has_c) x = x * cf.b + ((c0 + 8 * qd + j == r) ? e : 0.f);
             w8[j] = x;
           }
           d4[qd] = make_uint4(ptx::pack_bf16x2(w8[0], w8[1]), ptx::pack_bf16x2(w8[2], w8[3]),
@@ -289,8 +290,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
           float w8[8];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            w8[2 * j] = fmaf(g.ns.c, v[8 * qd + 2 * j], g.ns.b * ptx::bf16lo(uw[j]));
-            w8[2 * j + 1] = fmaf(g.ns.c, v[8 * qd + 2 * j + 1], g.ns.b * ptx::bf16hi(uw[j]));
+            w8[2 * j] = fmaf(cf.c, v[8 * qd + 2 * j], cf.b * ptx::bf16lo(uw[j]));
+            w8[2 * j + 1] = fmaf(cf.c, v[8 * qd + 2 * j + 1], cf.b * ptx::bf16hi(uw[j]));
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) w8[j] += (c0 + 8 * qd + j == r) ? e : 0.f;
@@ -310,9 +311,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, MINB)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             o[8 * qd + 2 * j] =
-                sc * fmaf(-e, ptx::bf16lo(uw[j]), fmaf(g.ns.a, xf[2 * j], v[8 * qd + 2 * j]));
+                sc * fmaf(-e, ptx::bf16lo(uw[j]), fmaf(cf.a, xf[2 * j], v[8 * qd + 2 * j]));
             o[8 * qd + 2 * j + 1] =
-                sc * fmaf(-e, ptx::bf16hi(uw[j]), fmaf(g.ns.a, xf[2 * j + 1], v[8 * qd + 2 * j + 1]));
+                sc * fmaf(-e, ptx::bf16hi(uw[j]), fmaf(cf.a, xf[2 * j + 1], v[8 * qd + 2 * j + 1]));
           }
         }
         if (!g.last) {
@@ -662,8 +663,8 @@ cudaError_t launch_ns_gemm_batch(const GTile* d_tiles, int n, int Hp, int Wp, co
     g.M = Hp; g.N = Hp; g.K = Wp;
     e = launch_gemm_bn<G_GRAM, false>(mXa[cur], mXb128[cur], mXb256[cur], g, n, stream);
     if (e != cudaSuccess) return e;
-    // G2: A A
-    if (ns.c != 0.f) {
+    // G2: A A (steps with c = 0 have no quadratic term)
+    if (step_coef(ns, k).has_c) {
       g.M = Hp; g.N = Hp; g.K = Hp;
       e = launch_gemm_bn<G_POLY, false>(mAa, mAb128, mAb256, g, n, stream);
       if (e != cudaSuccess) return e;

@@ -155,10 +155,6 @@ __global__ void __launch_bounds__(MTHREADS, 2)
   __nv_bfloat16* sx = reinterpret_cast<__nv_bfloat16*>(smem + warp * WARP_SMEM + U_BYTES);
   const uint32_t sx_addr = ptx::smem_u32(sx);
   const int T = ns.T, K = ns.K;
-  const float e = ns.a > 1.5f ? ns.a - 1.5f : 0.f;
-  const bool has_c = ns.c != 0.f;
-  // this lane's diagonal positions: F[bm][2bm][0 | 1] and F[bm][2bm+1][2 | 3]
-  const float ed0 = (g == 2 * t) ? e : 0.f, ed1 = (g == 2 * t + 1) ? e : 0.f;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * MW;
 
   for (int64_t tile = tile_begin + static_cast<int64_t>(blockIdx.x) * MW + warp; tile < tile_end;
@@ -264,6 +260,11 @@ __global__ void __launch_bounds__(MTHREADS, 2)
       scale_out = 1.f;
 #pragma unroll 1
       for (int k = 0; k < K; ++k) {
+        const StepCoef cf = step_coef(ns, k);  // this step's (a, b, c) and shift e
+        const float e = cf.e;
+        const bool has_c = cf.has_c;
+        // this lane's diagonal positions: F[bm][2bm][0 | 1] and F[bm][2bm+1][2 | 3]
+        const float ed0 = (g == 2 * t) ? e : 0.f, ed1 = (g == 2 * t + 1) ? e : 0.f;
         // R holds X here: its bf16 operand, and R = a X - e X_bf
         pack_a(R, XA);
 #pragma unroll
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(MTHREADS, 2)
               *reinterpret_cast<uint32_t*>(sx + row * XS + col) = XA[bm][kb][q];
             }
         {
-          const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
+          const uint64_t a2 = pk2(cf.a, cf.a), ne2 = pk2(-e, -e);
 #pragma unroll
           for (int bm = 0; bm < 2; ++bm)
 #pragma unroll
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(MTHREADS, 2)
           pack_a(D, AB);
           // ---- R_A = A_bf A_bf  ->  C = c A_bf A_bf + b A_bf + e I
           gram(AB, D);
-          const uint64_t c2 = pk2(ns.c, ns.c), b2 = pk2(ns.b, ns.b);
+          const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
 #pragma unroll
           for (int bm = 0; bm < 2; ++bm)
 #pragma unroll
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(MTHREADS, 2)
                 upk2(v, D[bm][bn][i], D[bm][bn][i + 1]);
               }
         } else {
-          scale_frag(D, ns.b * s2);
+          scale_frag(D, cf.b * s2);
         }
 #pragma unroll
         for (int bm = 0; bm < 2; ++bm) {

@@ -1,0 +1,518 @@
+// Tiled Newton-Schulz for 128 < T <= 256 on a CTA pair: every tile (zero-padded
+// to 256 x 256) stays on chip for all K steps, its products run on tcgen05 with
+// cta_group::2.
+//
+// Method ("Hierarchical Muon: Tiled Newton-Schulz Updates for Efficient Muon
+// Optimization", abstract, sentences 3-6): every tile X of a momentum-gradient
+// matrix is normalised and iterated K times with
+//   A = X X^T,  B = b_k A + c_k A^2,  X <- a_k X + B X,
+// independently of all other tiles; tile-size-specific kernels run the three
+// dense products per step. A 256 x 256 tile's fp32 iterate alone fills the
+// tensor memory of one SM, so a cluster of two CTAs (on two SMs) holds one
+// tile: CTA c owns rows [128 c, 128 c + 128) of every operand and accumulator,
+// and one thread of CTA 0 issues M = 256 products that read both CTAs' shared
+// memory and write both CTAs' tensor memory.
+//
+// Operands (CTA c, X = the tile, n-half c = columns [128 c, 128 c + 128)):
+//   X X^T  A: own rows of X, K = all 256 columns; B: the same rows (N split by CTA)
+//   A A^T  A and B: own rows of A_bf (A is symmetric)
+//   C X    A: own rows of C_bf; B: X restricted to the own n-half, K = all 256 rows,
+//          so each CTA needs the PEER's rows of its n-half: at the end of every
+//          step each CTA writes that block of its new X_bf into the peer's shared
+//          memory (distributed shared memory; no TMA multicast).
+// The two products' B operands sit at the same shared-memory offsets in both
+// CTAs, so X_bf is kept in four 128 x 128 buffers per CTA:
+//   B[c] = own rows x own half (X X^T, K-half c)  B[1-c] = own rows x other half
+//   B[2+c] = own rows x own half (C X, K-half c)  B[3-c] = peer rows x own half
+// Tensor memory per CTA (512 columns): R_A (256 columns) accumulates X X^T and
+// A A^T; R_X (256 columns) holds the fp32 iterate a X - e X_bf onto which C X_bf
+// is accumulated (the same rounding placement as the single-SM kernel).
+//
+// Threads per CTA: 16 warps (lane quarter = warp % 4, 64-column quarter =
+// warp / 4; 4 warps per scheduler leave 128 registers per thread) run the
+// prologue and the epilogues; warp 0 also allocates tensor memory, and thread 0
+// of CTA 0 issues the products. The input tile is read, momentum applied and
+// the output or weight update written by these threads directly from and to
+// global memory (rows pulled into L2 one tile ahead); wide tiles (fewer rows
+// than columns) are processed transposed, like the single-SM kernel.
+// Hand-off per product: both CTAs' threads meet at a named barrier; CTA 1's
+// thread 0 then arrives on CTA 0's peer_ready barrier; CTA 0's issuer
+// waits for that arrival and issues; completion is multicast to acc_full in both
+// CTAs. Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_util.cuh"
+
+namespace himuon {
+namespace {
+
+using namespace tile;
+
+constexpr int PT = 256;                       // padded tile side
+constexpr int NTHREADS = 512;                 // 16 warps, 4 per scheduler: 128 registers each
+constexpr int BAR_LINK = 1;                   // named barrier of all NTHREADS threads
+constexpr uint32_t TMEM_COLS = 512;
+
+// dynamic shared memory (offsets from the 1024-byte aligned base)
+__host__ __device__ constexpr uint32_t sm_b(int i) { return static_cast<uint32_t>(i) * 32768u; }
+constexpr uint32_t SM_C = 131072;             // 128 rows x 256 columns bf16: A_bf, then C_bf
+constexpr uint32_t SM_END = 196608;
+constexpr uint32_t SMEM_DYN = SM_END + 1024;
+
+struct PairCtl {
+  uint64_t acc_full;     // the pair's last product is complete (multicast commit)
+  uint64_t peer_ready;   // the peer CTA has finished its part of a hand-off
+  uint64_t drain;        // abort path: every issued product has completed
+  uint32_t tmem_base;
+  int abort_flag;
+  float part[16];        // per warp: sum of squares of its elements
+  float part_peer;       // the peer CTA's sum (written by the peer)
+};
+
+// bounded wait on a local mbarrier whose arrivals may come from the peer CTA
+__device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile int* abort_flag, int* err) {
+  if (ptx::mbar_try_wait_cluster(bar, parity, 0u)) return;
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait_cluster(bar, parity, 20000u)) {
+    if (*abort_flag) return;
+    if (ptx::globaltimer() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// 32 bf16 values -> 4 x 16-byte chunks of row r, columns [c, c + 32), of a
+// swizzled bf16 buffer in the PEER's shared memory (cluster address of its base)
+__device__ __forceinline__ void st_bf16_32_remote(uint32_t rbase, int r, int c,
+                                                  const uint32_t (&pkd)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    ptx::st_cluster_v4(rbase + bf_off(r, (c >> 3) + q), pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2],
+                       pkd[4 * q + 3]);
+}
+
+template <bool STEP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    ns_pair_kernel(const MatDesc* __restrict__ descs, int ndesc, int64_t tile_begin,
+                   int64_t tile_end, NSArgs ns, StepArgs st, uint64_t wait_ns,
+                   int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ PairCtl ctl;
+
+  const uint32_t sbase = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t c = ptx::cluster_ctarank();     // 0: issues the products
+  const uint32_t peer = c ^ 1u;
+  volatile int* abort_flag = &ctl.abort_flag;
+  const uint32_t b_acc = ptx::smem_u32(&ctl.acc_full);
+  const uint32_t b_peer = ptx::smem_u32(&ctl.peer_ready);
+  const uint32_t b_drain = ptx::smem_u32(&ctl.drain);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b_acc, 1);
+    ptx::mbar_init(b_peer, 1);
+    ptx::mbar_init(b_drain, 1);
+    ptx::fence_mbar_init();
+    ctl.abort_flag = 0;
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&ctl.tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();           // both CTAs' barriers exist before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tbase = ctl.tmem_base;
+
+  const int K = ns.K;
+  const bool issuer = (c == 0 && threadIdx.x == 0);
+  const int q = warp & 3;                         // TMEM lane quarter
+  const int cq = warp >> 2;                       // 64-column quarter
+  const int r = 32 * q + lane;                    // local row = TMEM lane
+  const int xr = 128 * static_cast<int>(c) + r;   // row of the (processed) tile
+  const int xc0 = 64 * cq;                        // first tile column of this thread
+  const bool own = (cq >> 1) == static_cast<int>(c);
+  const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+  const uint32_t t_a = tbase + lane_off;          // R_A, columns 0..255
+  const uint32_t t_x = tbase + lane_off + 256u;   // R_X, columns 256..511
+  const uint32_t sc = sbase + SM_C;
+  // this thread's X_bf buffers: own half -> B[c] and B[2+c] (local); other half
+  // -> B[1-c] (local) and B[2+c] of the peer
+  const uint32_t xb1 = sbase + sm_b(own ? static_cast<int>(c) : 1 - static_cast<int>(c));
+  const uint32_t xb2_local = sbase + sm_b(2 + static_cast<int>(c));
+  const uint32_t xb2_remote = ptx::mapa_shared(sbase + sm_b(2 + static_cast<int>(c)), peer);
+
+  uint32_t acc_ph = 0, pr_ph = 0;
+  bool issued = false;
+
+  // product p of the tile (0: X X^T -> R_A; 1: A A^T -> R_A; 2: C X onto R_X)
+  auto issue = [&](int p) {
+    if (!issuer || *abort_flag) return;
+    constexpr uint32_t IDESC_KK = ptx::idesc_bf16_f32(256, 256, false, false);
+    constexpr uint32_t IDESC_KM = ptx::idesc_bf16_f32(256, 256, false, true);
+    ptx::tc_fence_after();
+    const uint32_t dcol = tbase + (p == 2 ? 256u : 0u);
+#pragma unroll
+    for (int kk = 0; kk < PT / 16; ++kk) {
+      uint64_t ad, bd;
+      if (p == 0) {
+        ad = ptx::sdesc_sw128(sbase + sm_b(kk >> 3) + ((kk & 7) >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        bd = ad;
+      } else {
+        ad = ptx::sdesc_sw128(sc + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+        bd = (p == 1) ? ad
+                      : ptx::sdesc_sw128(sbase + sm_b(2 + (kk >> 3)) + (kk & 7) * 16 * 128, 16384, 1024);
+      }
+      ptx::umma_bf16_pair(dcol, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, (p == 2 || kk > 0) ? 1u : 0u);
+    }
+    ptx::umma_commit_pair_mc(b_acc, 0x3);
+    issued = true;
+  };
+
+  // Hand-off after an epilogue: operands written (local and peer shared memory,
+  // tensor memory) -> product p. CTA 0's issuer waits for CTA 1's arrival.
+  auto hand_over = [&](bool tmem_written, int p) {
+    if (tmem_written) ptx::tmem_wait_st();
+    ptx::fence_proxy_async_all();
+    ptx::tc_fence_before();
+    named_sync(BAR_LINK, NTHREADS);
+    if (c == 1) {
+      if (threadIdx.x == 0 && !*abort_flag) ptx::mbar_arrive_cluster(ptx::mapa_shared(b_peer, 0));
+    } else {
+      if (issuer) {
+        wait_cluster(b_peer, pr_ph, wait_ns, abort_flag, err);
+        issue(p);
+      }
+      pr_ph ^= 1u;
+    }
+  };
+
+  auto wait_acc = [&]() {
+    wait_bar(b_acc, acc_ph, wait_ns, abort_flag, err);
+    acc_ph ^= 1u;
+    ptx::tc_fence_after();
+  };
+
+  const int T = ns.T;
+  const int64_t ncl = gridDim.x >> 1;
+#pragma unroll 1
+  for (int64_t tile = tile_begin + (blockIdx.x >> 1); tile < tile_end; tile += ncl) {
+    const int mi = find_matrix(descs, ndesc, tile);
+    const MatDesc& d = descs[mi];
+    const int64_t lt = tile - d.tile_start;
+    const int i0 = static_cast<int>(lt / d.tiles_w) * T, j0 = static_cast<int>(lt % d.tiles_w) * T;
+    const int h = min(T, d.H - i0), w = min(T, d.W - j0);
+    const bool tr = h < w;                 // processed transposed: X = tile^T
+    const int xh = tr ? w : h, xw = tr ? h : w;
+    const bool in32 = d.flags & F_IN_FP32, out32 = d.flags & F_OUT_FP32;
+    const bool m16 = d.flags & F_M_BF16;
+    const int ies = in32 ? 4 : 2, oes = out32 ? 4 : 2, mes = m16 ? 2 : 4;
+
+    // ---- prologue: U (momentum applied for a step, M written back) into
+    // R_X = a U - e U_bf and the X_bf buffers; sums of squares
+    float ssq = 0.f;
+    {
+      const StepCoef cf0 = step_coef(ns, 0);
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        const int xc = xc0 + 32 * ch;
+        const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
+        float u[32];
+        if (!tr) {
+          const char* gp = gptr(d.in, d.ld_in, i0 + xr, j0, in32);
+          const bool vin = (d.flags & F_IN_VEC) && ((j0 + xc) * ies) % 16 == 0;
+          gload32(gp, xc, n, in32, vin, u);
+          if (STEP) {
+            char* mp = gptr(d.mom, d.ld_mom, i0 + xr, j0, !m16);
+            const bool vm = (d.flags & F_M_VEC) && ((j0 + xc) * mes) % 16 == 0;
+            float mv[32];
+            gload32(mp, xc, n, !m16, vm, mv);
+            const uint64_t mu2 = pk2(st.mu, st.mu);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint64_t mn = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(u[j], u[j + 1]));
+              upk2(mn, mv[j], mv[j + 1]);
+              if (st.nesterov) upk2(fma2(mu2, mn, pk2(u[j], u[j + 1])), u[j], u[j + 1]);
+              else upk2(mn, u[j], u[j + 1]);
+            }
+            if (n > 0) gstore32(mp, xc, n, !m16, vm, mv);
+          }
+        } else {
+          // X = tile^T: element (xr, xc + j) is G[i0 + xc + j][j0 + xr]; the
+          // lanes of a warp read consecutive columns of one row
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float x = 0.f;
+            if (j < n) {
+              const char* gp = gptr(d.in, d.ld_in, i0 + xc + j, j0 + xr, in32);
+              x = in32 ? *reinterpret_cast<const float*>(gp)
+                       : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gp));
+              if (STEP) {
+                char* mp = gptr(d.mom, d.ld_mom, i0 + xc + j, j0 + xr, !m16);
+                const float m = m16 ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(mp))
+                                    : *reinterpret_cast<const float*>(mp);
+                const float mn = fmaf(st.mu, m, x);
+                if (m16) *reinterpret_cast<__nv_bfloat16*>(mp) = __float2bfloat16_rn(mn);
+                else *reinterpret_cast<float*>(mp) = mn;
+                x = st.nesterov ? fmaf(st.mu, mn, x) : mn;
+              }
+            }
+            u[j] = x;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ssq = fmaf(u[j], u[j], ssq);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(u[2 * j], u[2 * j + 1]);
+        const int cl = xc & 127;                     // column within the 128-wide buffer
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd)
+          ptx::st_shared_v4(xb1 + bf_off(r, (cl >> 3) + qd), pkd[4 * qd], pkd[4 * qd + 1],
+                            pkd[4 * qd + 2], pkd[4 * qd + 3]);
+        if (own) {
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd)
+            ptx::st_shared_v4(xb2_local + bf_off(r, (cl >> 3) + qd), pkd[4 * qd], pkd[4 * qd + 1],
+                              pkd[4 * qd + 2], pkd[4 * qd + 3]);
+        } else {
+          st_bf16_32_remote(xb2_remote, r, cl, pkd);
+        }
+        const uint64_t a2 = pk2(cf0.a, cf0.a), ne2 = pk2(-cf0.e, -cf0.e);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint64_t x = fma2(a2, pk2(u[2 * j], u[2 * j + 1]),
+                                  mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
+          upk2(x, u[2 * j], u[2 * j + 1]);
+        }
+        ptx::tmem_st32(t_x + xc, u);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+      if (lane == 0) ctl.part[warp] = ssq;
+
+      // the next tile's rows of this thread into L2 (G, M and W for a step)
+      const int64_t nt = tile + ncl;
+      if (nt < tile_end) {
+        const MatDesc& dn = descs[find_matrix(descs, ndesc, nt)];
+        const int64_t nlt = nt - dn.tile_start;
+        const int ni0 = static_cast<int>(nlt / dn.tiles_w) * T, nj0 = static_cast<int>(nlt % dn.tiles_w) * T;
+        const int nh = min(T, dn.H - ni0), nw = min(T, dn.W - nj0);
+        if (nh >= nw && xr < nh && xc0 < nw) {
+          const bool n32 = dn.flags & F_IN_FP32;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr(dn.in, dn.ld_in, ni0 + xr, nj0 + xc0, n32)));
+          if (STEP) {
+            const bool nm32 = !(dn.flags & F_M_BF16), nw32 = dn.flags & F_OUT_FP32;
+            const char* mp = gptr(dn.mom, dn.ld_mom, ni0 + xr, nj0 + xc0, nm32);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(mp));
+            if (nm32) asm volatile("prefetch.global.L2 [%0];" ::"l"(mp + 128));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr(dn.out, dn.ld_out, ni0 + xr, nj0 + xc0, nw32)));
+          }
+        }
+      }
+    }
+    ptx::tmem_wait_st();
+    ptx::fence_proxy_async_all();
+    ptx::tc_fence_before();
+    named_sync(BAR_LINK, NTHREADS);
+    // tile norm: each CTA's sum (fixed order) goes to the peer, with an arrival
+    float part_self = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) part_self += ctl.part[i];
+    if (threadIdx.x == 0 && !*abort_flag) {
+      ptx::st_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&ctl.part_peer), peer), part_self);
+      ptx::mbar_arrive_cluster(ptx::mapa_shared(b_peer, peer));
+    }
+    wait_cluster(b_peer, pr_ph, wait_ns, abort_flag, err);
+    pr_ph ^= 1u;
+    named_sync(BAR_LINK, NTHREADS);        // no thread of CTA 0 lags a phase behind the issuer
+    const float tot = (c == 0) ? part_self + ctl.part_peer : ctl.part_peer + part_self;
+    float sc_t = 1.f;
+    if (ns.norm == NORM_TILE) sc_t = 1.f / (sqrtf(tot) + ns.eps);
+    else if (ns.norm == NORM_MATRIX) sc_t = d.norm_scale;
+    const float s2 = sc_t * sc_t;
+    ptx::tc_fence_after();
+    issue(0);                              // -> X X^T
+
+#pragma unroll 1
+    for (int k = 0; k < K; ++k) {
+      const StepCoef cf = step_coef(ns, k);
+      const float e = cf.e;
+      // ---- E1: A = X X^T (R_A) -> A_bf = bf16(s^2 R_A), or C = b A + e I when c = 0
+      {
+        wait_acc();
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_a + xc, v);
+          if (cf.has_c) {
+            if (k == 0) scale32(v, s2);
+          } else {
+            scale32(v, k == 0 ? cf.b * s2 : cf.b);
+            if ((xr >> 5) == (xc >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
+            }
+          }
+          uint32_t pkd[16];
+          st_bf16_32(sc, r, xc, v, pkd);
+        }
+      }
+      hand_over(false, cf.has_c ? 1 : 2);
+
+      if (cf.has_c) {
+        // ---- E2: R_A = A_bf A_bf^T -> C = c R_A + b A_bf + e I (B at the rounded A_bf)
+        {
+          wait_acc();
+#pragma unroll 1
+          for (int ch = 0; ch < 2; ++ch) {
+            const int xc = xc0 + 32 * ch;
+            float v[32], av[32];
+            ptx::tmem_ld32_sync(t_a + xc, v);
+            ld_bf16_32(sc, r, xc, av);
+            const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint64_t x = fma2(c2, pk2(v[j], v[j + 1]), mul2(b2, pk2(av[j], av[j + 1])));
+              upk2(x, v[j], v[j + 1]);
+            }
+            if ((xr >> 5) == (xc >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
+            }
+            uint32_t pkd[16];
+            st_bf16_32(sc, r, xc, v, pkd);
+          }
+        }
+        hand_over(false, 2);
+      }
+
+      // ---- E3: R_X = X' (on the first step X_1 / s): the next step's operands,
+      // or the output / weight update
+      const bool last = (k + 1 == K);
+      {
+        wait_acc();
+        const StepCoef cfn = step_coef(ns, last ? k : k + 1);
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_x + xc, v);
+          if (k == 0) scale32(v, sc_t);
+          if (!last) {
+            uint32_t pkd[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            const int cl = xc & 127;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd)
+              ptx::st_shared_v4(xb1 + bf_off(r, (cl >> 3) + qd), pkd[4 * qd], pkd[4 * qd + 1],
+                                pkd[4 * qd + 2], pkd[4 * qd + 3]);
+            if (own) {
+#pragma unroll
+              for (int qd = 0; qd < 4; ++qd)
+                ptx::st_shared_v4(xb2_local + bf_off(r, (cl >> 3) + qd), pkd[4 * qd], pkd[4 * qd + 1],
+                                  pkd[4 * qd + 2], pkd[4 * qd + 3]);
+            } else {
+              st_bf16_32_remote(xb2_remote, r, cl, pkd);
+            }
+            const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
+                                      mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
+              upk2(x, v[2 * j], v[2 * j + 1]);
+            }
+            ptx::tmem_st32(t_x + xc, v);
+            continue;
+          }
+          // last step: out = X' (NS map), or W <- wd W - lr s X' (step)
+          const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
+          if (n == 0) continue;
+          if (!tr) {
+            char* op = gptr(d.out, d.ld_out, i0 + xr, j0, out32);
+            const bool vo = (d.flags & F_OUT_VEC) && ((j0 + xc) * oes) % 16 == 0;
+            if (STEP) {
+              float wv[32];
+              gload32(op, xc, n, out32, vo, wv);
+              const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale), wdf = pk2(st.wd_factor, st.wd_factor);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2)
+                upk2(fma2(nls, pk2(v[j], v[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1]))), wv[j], wv[j + 1]);
+              gstore32(op, xc, n, out32, vo, wv);
+            } else {
+              gstore32(op, xc, n, out32, vo, v);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j >= n) break;
+              char* op = gptr(d.out, d.ld_out, i0 + xc + j, j0 + xr, out32);
+              float o = v[j];
+              if (STEP) {
+                const float wv = out32 ? *reinterpret_cast<const float*>(op)
+                                       : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(op));
+                o = fmaf(-d.upd_scale, o, wv * st.wd_factor);
+              }
+              if (out32) *reinterpret_cast<float*>(op) = o;
+              else *reinterpret_cast<__nv_bfloat16*>(op) = __float2bfloat16_rn(o);
+            }
+          }
+        }
+      }
+      if (!last) hand_over(true, 0);       // -> next X X^T
+    }
+  }
+
+  // ---- teardown: every product this CTA issued has completed, then both CTAs
+  // leave together (the peer writes into this CTA's shared memory)
+  if (issued && *abort_flag) {
+    ptx::umma_commit_pair_mc(b_drain, 0x1);
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(b_drain, 0) && ptx::globaltimer() - t0 < wait_ns) {
+    }
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tbase, TMEM_COLS);
+  }
+}
+
+template <bool STEP>
+cudaError_t launch_p(const MatDesc* descs, int ndesc, int64_t tile_begin, int64_t tile_end,
+                     const NSArgs& ns, const StepArgs& st, uint64_t wait_ns, int* err, int num_sms,
+                     cudaStream_t stream) {
+  const int64_t tiles = tile_end - tile_begin;
+  const int clusters = static_cast<int>(std::min<int64_t>(tiles, std::max(1, num_sms / 2)));
+  cudaError_t e = cudaFuncSetAttribute(ns_pair_kernel<STEP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+  if (e != cudaSuccess) return e;
+  ns_pair_kernel<STEP><<<2 * clusters, NTHREADS, SMEM_DYN, stream>>>(descs, ndesc, tile_begin,
+                                                                     tile_end, ns, st, wait_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ns_pair(const MatDesc* descs, int ndesc, int64_t tile_begin, int64_t tile_end,
+                           const NSArgs& ns, const StepArgs& st, uint64_t wait_ns, int* err,
+                           int num_sms, cudaStream_t stream) {
+  if (tile_end <= tile_begin) return cudaSuccess;
+  if (ns.T <= 128 || ns.T > PT || ns.K < 1) return cudaErrorInvalidValue;
+  return st.enabled ? launch_p<true>(descs, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream)
+                    : launch_p<false>(descs, ndesc, tile_begin, tile_end, ns, st, wait_ns, err, num_sms, stream);
+}
+
+}  // namespace himuon

@@ -47,9 +47,12 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_util.cuh"
 
 namespace himuon {
 namespace {
+
+using namespace tile;
 
 constexpr int NWARPS = 20;
 constexpr int NTHREADS = NWARPS * 32;
@@ -83,214 +86,10 @@ struct Ctl {
   float info_s[4];
   int ticket;             // next stage to hand to a free slot
   int ticket_s[2];        // the stage each slot took
+  // per slot and stacked tile: where its -lr s O goes by TMA reduce-add
+  // (matrix or -1, origin, width); copied from info_* when the slot takes a stage
+  int red_mi[2][2], red_i0[2][2], red_j0[2][2], red_w[2][2];
 };
-
-// ------------------------------------------------------------------ layouts
-// bf16 tile: element (r, c) in block c / 64, 16-byte chunk ((c % 64) / 8) ^ (r % 8).
-__device__ __forceinline__ uint32_t bf_off(int r, int c8) {   // c8 = c / 8
-  return static_cast<uint32_t>((c8 >> 3) * 16384 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
-}
-// fp32 tile: element (r, c) in block c / 32, 16-byte chunk ((c % 32) / 4) ^ (r % 8).
-__device__ __forceinline__ uint32_t f32_off(int r, int c4) {  // c4 = c / 4
-  return static_cast<uint32_t>((c4 >> 3) * 16384 + r * 128 + (((c4 & 7) ^ (r & 7)) << 4));
-}
-
-// ------------------------------------------------------------------ packed fp32 pairs
-__device__ __forceinline__ uint64_t pk2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-// v[j] *= s for 32 values, in pairs
-__device__ __forceinline__ void scale32(float (&v)[32], float s) {
-  const uint64_t ss = pk2(s, s);
-#pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    uint64_t x = mul2(pk2(v[j], v[j + 1]), ss);
-    upk2(x, v[j], v[j + 1]);
-  }
-}
-
-// 32 fp32 -> 16 packed bf16x2 -> 4 x 16-byte chunks of a bf16 tile row
-__device__ __forceinline__ void st_bf16_32(uint32_t tile, int r, int c, const float (&v)[32],
-                                           uint32_t (&pkd)[16]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    ptx::st_shared_v4(tile + bf_off(r, (c >> 3) + q), pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2],
-                      pkd[4 * q + 3]);
-}
-
-__device__ __forceinline__ void ld_bf16_32(uint32_t tile, int r, int c, float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u = ptx::ld_shared_v4(tile + bf_off(r, (c >> 3) + q));
-    v[8 * q + 0] = ptx::bf16lo(u.x); v[8 * q + 1] = ptx::bf16hi(u.x);
-    v[8 * q + 2] = ptx::bf16lo(u.y); v[8 * q + 3] = ptx::bf16hi(u.y);
-    v[8 * q + 4] = ptx::bf16lo(u.z); v[8 * q + 5] = ptx::bf16hi(u.z);
-    v[8 * q + 6] = ptx::bf16lo(u.w); v[8 * q + 7] = ptx::bf16hi(u.w);
-  }
-}
-
-__device__ __forceinline__ void ld_f32_32(uint32_t tile, int r, int c, float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint4 u = ptx::ld_shared_v4(tile + f32_off(r, (c >> 2) + q));
-    v[4 * q + 0] = __uint_as_float(u.x); v[4 * q + 1] = __uint_as_float(u.y);
-    v[4 * q + 2] = __uint_as_float(u.z); v[4 * q + 3] = __uint_as_float(u.w);
-  }
-}
-
-__device__ __forceinline__ void st_f32_32(uint32_t tile, int r, int c, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    ptx::st_shared_v4(tile + f32_off(r, (c >> 2) + q), __float_as_uint(v[4 * q]),
-                      __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
-                      __float_as_uint(v[4 * q + 3]));
-}
-
-// single elements of the staging tiles (for tiles processed transposed)
-__device__ __forceinline__ float f32_at(uint32_t tile, int r, int c) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(tile + f32_off(r, c >> 2) + (c & 3) * 4));
-  return v;
-}
-__device__ __forceinline__ float bf16_at(uint32_t tile, int r, int c) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(tile + bf_off(r, c >> 3) + (c & 7) * 2));
-  return __uint_as_float(static_cast<uint32_t>(v) << 16);
-}
-
-__device__ __forceinline__ void f32_put(uint32_t tile, int r, int c, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(tile + f32_off(r, c >> 2) + (c & 3) * 4), "f"(v) : "memory");
-}
-
-// ------------------------------------------------------------------ global row segments
-// 32 elements from column c0 of a row, n of them valid (0..32); vector access
-// when all 32 are valid and the row allows 16-byte access.
-__device__ __forceinline__ void gload32(const void* rowp, int c0, int n, bool fp32, bool vec,
-                                        float (&v)[32]) {
-  if (n >= 32 && vec) {
-    if (fp32) {
-      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(rowp) + c0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 f = p[q];
-        v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-      }
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(rowp) + c0);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 u = p[q];
-        v[8 * q + 0] = ptx::bf16lo(u.x); v[8 * q + 1] = ptx::bf16hi(u.x);
-        v[8 * q + 2] = ptx::bf16lo(u.y); v[8 * q + 3] = ptx::bf16hi(u.y);
-        v[8 * q + 4] = ptx::bf16lo(u.z); v[8 * q + 5] = ptx::bf16hi(u.z);
-        v[8 * q + 6] = ptx::bf16lo(u.w); v[8 * q + 7] = ptx::bf16hi(u.w);
-      }
-    }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float x = 0.f;
-    if (j < n)
-      x = fp32 ? static_cast<const float*>(rowp)[c0 + j]
-               : __bfloat162float(static_cast<const __nv_bfloat16*>(rowp)[c0 + j]);
-    v[j] = x;
-  }
-}
-
-__device__ __forceinline__ void gstore32(void* rowp, int c0, int n, bool fp32, bool vec,
-                                         const float (&v)[32]) {
-  if (n >= 32 && vec) {
-    if (fp32) {
-      float4* p = reinterpret_cast<float4*>(static_cast<float*>(rowp) + c0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-      uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(rowp) + c0);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        p[q] = make_uint4(ptx::pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                          ptx::pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                          ptx::pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                          ptx::pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-    }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (j < n) {
-      if (fp32) static_cast<float*>(rowp)[c0 + j] = v[j];
-      else static_cast<__nv_bfloat16*>(rowp)[c0 + j] = __float2bfloat16_rn(v[j]);
-    }
-  }
-}
-
-__device__ __forceinline__ char* gptr(const void* base, int64_t ld, int64_t row, int64_t col,
-                                      bool fp32) {
-  return const_cast<char*>(static_cast<const char*>(base)) + (row * ld + col) * (fp32 ? 4 : 2);
-}
-
-// ------------------------------------------------------------------ bounded waits
-// Waits for the phase of `bar` with the given parity. Gives up once the CTA
-// has aborted or after limit_ns (then records the time-out and aborts the CTA).
-// After an abort every wait returns at once, so all roles run to the end.
-// try_wait with a suspend-time hint: the waiting thread sleeps until the phase
-// completes or about 20 us pass, instead of spinning on the issue slots that
-// the epilogue warps of its scheduler need.
-__device__ __forceinline__ bool try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                         volatile int* abort_flag, int* err) {
-  if (ptx::mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = ptx::globaltimer();
-  while (!try_wait_sleep(bar, parity)) {
-    if (*abort_flag) return;
-    if (ptx::globaltimer() - t0 > limit_ns) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, DEV_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void tensormap_acquire(const void* map) {
-  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
-}
 
 // Tile of a launch's flat list: matrix, origin and valid extent.
 struct TileRef {
@@ -314,6 +113,31 @@ __device__ __forceinline__ int tile_format(int flags) {
   if (!(flags & F_TMA)) return FMT_U32;
   if (STEP) return FMT_G16M32;
   return (flags & F_IN_FP32) ? FMT_U32 : FMT_G16;
+}
+
+// One thread adds the stage's -lr s O tiles (bf16, in the slot's sC buffer, the
+// swizzled layout of the TMA box) to W by TMA reduce-add, one box of 64
+// columns x T rows per 64 valid columns. Returns whether a bulk group was
+// committed (it must finish reading sC before sC is written again).
+template <int T>
+__device__ __noinline__ bool issue_w_reduce(const Ctl& ctl, int s, const CUtensorMap* maps,
+                                            uint32_t sc) {
+  constexpr int TPS = 128 / T;
+  bool any = false;
+  for (int u = 0; u < TPS; ++u) {
+    const int m_u = ctl.red_mi[s][u];
+    if (m_u < 0) continue;
+    const CUtensorMap* mw = maps + 3 * m_u + 2;
+    tensormap_acquire(mw);
+    for (int b = 0; b < T / 64; ++b) {
+      if (64 * b >= ctl.red_w[s][u]) break;            // box wholly right of the matrix
+      ptx::tma_reduce_add_2d(mw, sc + b * 16384 + u * T * 128, ctl.red_j0[s][u] + 64 * b,
+                             ctl.red_i0[s][u]);
+    }
+    any = true;
+  }
+  if (any) ptx::bulk_commit();
+  return any;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -365,8 +189,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int64_t stride_tiles = static_cast<int64_t>(gridDim.x) * TPS;
   const int64_t first_tile = tile_begin + static_cast<int64_t>(blockIdx.x) * TPS;
   // e = a - min(a, 1.5): part of a I moved into the bf16 operand C = B + e I
-  const float e = ns.a > 1.5f ? ns.a - 1.5f : 0.f;
-  const bool has_c = ns.c != 0.f;
+  // (per NS step: step k uses coefficients (a_k, b_k, c_k))
+  const StepCoef cf0 = step_coef(ns, 0);
 
   if (warp < 4) {
     // =============================================================== loader
@@ -386,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int u = 0; u < TPS; ++u) {
         if (pend_mi[u] < 0) continue;
         if (!*abort_flag) {
-          const CUtensorMap* mm = maps + 2 * pend_mi[u] + 1;
+          const CUtensorMap* mm = maps + 3 * pend_mi[u] + 1;
           for (int b = 0; b < T / 32; ++b) {
             if (32 * b >= pend_w[u]) break;     // box wholly right of the matrix
             ptx::tma_store_2d(mm, sbase + SM_S0 + b * 16384 + u * T * 128, pend_j0[u] + 32 * b,
@@ -436,7 +260,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < TPS; ++u) {      // G first: its buffer holds nothing to store
           if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
-          const CUtensorMap* mg = maps + 2 * ref[u].mi;
+          const CUtensorMap* mg = maps + 3 * ref[u].mi;
           if (ref[u].mi != last_mi) {
             tensormap_acquire(mg);
             if (STEP) tensormap_acquire(mg + 1);
@@ -458,7 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int u = 0; u < TPS; ++u) {
             if (ref[u].mi < 0 || !(descs[ref[u].mi].flags & F_TMA)) continue;
-            const CUtensorMap* mm = maps + 2 * ref[u].mi + 1;
+            const CUtensorMap* mm = maps + 3 * ref[u].mi + 1;
             for (int b = 0; b < T / 32; ++b)
               ptx::tma_load_2d(sbase + SM_S0 + b * 16384 + u * T * 128, mm, ref[u].j0 + 32 * b,
                                ref[u].i0, b_loaded);
@@ -556,6 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int pw = 1 + s;
     const bool issuer = (ws == pw && lane == 0);
     bool issued = false;
+    bool reduce_pending = false;   // issuer: a TMA reduce-add still reads sC
 
     // Product p of this slot (0: X X^T -> R_A; 1: A A onto R_A; 2: C X onto R_X),
     // one 128 x T x T MMA per stacked tile, completion signalled on acc_full[s].
@@ -731,6 +556,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int th = ctl.info_h[t], tw = ctl.info_w[t];
       const int fmt = ctl.info_fmt[t];
       const float s_info = ctl.info_s[t];
+      // the stage's tiles whose weights take the TMA reduce-add, copied now: the
+      // loader rewrites ctl.info_* for the next stage once staging is released
+      if (STEP && issuer) {
+#pragma unroll
+        for (int u = 0; u < TPS; ++u) {
+          const int m_u = ctl.info_mi[u];
+          const bool ok = m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u] && (descs[m_u].flags & F_W_TMA);
+          ctl.red_mi[s][u] = ok ? m_u : -1;
+          ctl.red_i0[s][u] = ctl.info_i0[u];
+          ctl.red_j0[s][u] = ctl.info_j0[u];
+          ctl.red_w[s][u] = ctl.info_w[u];
+        }
+      }
 
       // ---- prologue: staging -> sX = U_bf and R_X = a U - e U_bf, with the sum
       // of squares of U for the normalisation. The input itself (exact for bf16
@@ -742,7 +580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // the bf16 rounding of X enters B X through a projection that averages
       // it over the long side, instead of elementwise.
       const bool tr = th < tw;
-      if (STEP && mi >= 0 && !tr && rl < th && cbase < tw) {
+      if (STEP && mi >= 0 && !tr && !(descs[mi].flags & F_W_TMA) && rl < th && cbase < tw) {
         // the weights this thread updates at the end of the tile: pull them into
         // L2 now, so that the final update does not wait on DRAM
         const MatDesc& d = descs[mi];
@@ -762,7 +600,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (K == 0) continue;
         uint32_t pkd[16];
         st_bf16_32(sx, r, c, y, pkd);
-        const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
+        const uint64_t a2 = pk2(cf0.a, cf0.a), ne2 = pk2(-cf0.e, -cf0.e);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           uint64_t x = fma2(a2, pk2(y[2 * j], y[2 * j + 1]),
@@ -805,6 +643,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (issuer) mbar_arrive(b_empty);
         continue;
       }
+      if (reduce_pending) {                // sC is rewritten after the first product
+        ptx::bulk_wait_read0();
+        reduce_pending = false;
+      }
       ptx::tmem_wait_st();
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
@@ -816,6 +658,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 #pragma unroll 1
       for (int k = 0; k < K; ++k) {
+        const StepCoef cf = step_coef(ns, k);
+        const float e = cf.e;
+        const bool has_c = cf.has_c;
         // ---- E1: A = X X^T in R_A
         wait_acc();
 #pragma unroll 1
@@ -828,7 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (k == 0) scale32(v, s2);              // A = s^2 U_bf U_bf^T
             st_bf16_32(sc, r, c, v, pkd);            // A_bf
           } else {
-            scale32(v, k == 0 ? ns.b * s2 : ns.b);   // C = b A + e I
+            scale32(v, k == 0 ? cf.b * s2 : cf.b);   // C = b A + e I
             if ((rl >> 5) == (c >> 5)) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
@@ -851,7 +696,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float v[32], av[32];
             ptx::tmem_ld32_sync(t_a + c, v);
             ld_bf16_32(sc, r, c, av);
-            const uint64_t c2 = pk2(ns.c, ns.c), b2 = pk2(ns.b, ns.b);
+            const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
               uint64_t x = fma2(c2, pk2(v[j], v[j + 1]), mul2(b2, pk2(av[j], av[j + 1])));
@@ -867,9 +712,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           hand_over(true, false, 2);       // -> C X
         }
 
-        // ---- E3: R_X = X' (on the first step X_1 / s)
+        // ---- E3: R_X = X' (on the first step X_1 / s); the next step's
+        // a X' - e X'_bf takes that step's coefficients
         wait_acc();
         const bool last = (k + 1 == K);
+        const StepCoef cfn = step_coef(ns, last ? k : k + 1);
+        // step: W += -lr s O by a TMA reduce-add from sC (bf16 W, no decay)
+        const bool w_red = STEP && last && mi >= 0 && !tr && (descs[mi].flags & F_W_TMA);
 #pragma unroll 1
         for (int ch = 0; ch < nch; ++ch) {
           const int c = cbase + 32 * ch;
@@ -877,11 +726,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ptx::tmem_ld32_sync(t_x + c, v);
           if (k == 0) scale32(v, sc_t);
           if (last) {
-            if (mi >= 0) emit(descs[mi], i0, j0, th, tw, tr, c, v);
+            if (w_red) {
+              scale32(v, -descs[mi].upd_scale);     // -lr s O, added to W by TMA below
+              uint32_t pkd[16];
+              st_bf16_32(sc, r, c, v, pkd);
+            } else if (mi >= 0) {
+              emit(descs[mi], i0, j0, th, tw, tr, c, v);
+            }
           } else {
             uint32_t pkd[16];
             st_bf16_32(sx, r, c, v, pkd);
-            const uint64_t a2 = pk2(ns.a, ns.a), ne2 = pk2(-e, -e);
+            const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
@@ -893,7 +748,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!last) hand_over(true, true, 0);   // -> next X X^T
       }
+      if (STEP) {
+        // the stage's -lr s O tiles are in sC: one thread adds them to W
+        ptx::fence_proxy_async_smem();
+        named_sync(2 + s, SLOT_THREADS);
+        if (issuer && !*abort_flag && issue_w_reduce<T>(ctl, s, maps, sc)) reduce_pending = true;
+      }
     }
+    if (reduce_pending) ptx::bulk_wait0();     // the reduces have completed before exit
 
     if (issued && *abort_flag) {
       // let every MMA this slot issued finish before tensor memory is released
