@@ -271,16 +271,17 @@ def check_update(W_gpu, W0, W_ref, tol):
     assert np.linalg.norm(d_gpu - d_ref) <= tol * np.linalg.norm(d_ref)
 
 
-@pytest.mark.parametrize("path,wdtype", [("tensor", torch.bfloat16), ("tensor", torch.float32),
-                                         ("fp32", torch.float32)])
-def test_step_matches_oracle(path, wdtype):
+@pytest.mark.parametrize("path,wdtype,T", [("tensor", torch.bfloat16, 128), ("tensor", torch.float32, 128),
+                                           ("tensor", torch.bfloat16, 64), ("tensor", torch.float32, 64),
+                                           ("fp32", torch.float32, 128)])
+def test_step_matches_oracle(path, wdtype, T):
     shapes = [(768, 768), (3072, 768), (300, 530)]
     Ws, Gs, Ms = _step_case(shapes, 50, wdtype=wdtype)
     W0 = [f64(w) for w in Ws]
     M0 = [f64(m) for m in Ms]
-    hm.step(Ws, Gs, Ms, 128, 5, lr=0.02, mu=0.95, nesterov=True, path=path)
+    hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95, nesterov=True, path=path)
     for i, (H, W) in enumerate(shapes):
-        Wn, Mn, O = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], 128, 5, lr=0.02, mu=0.95)
+        Wn, Mn, O = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], T, 5, lr=0.02, mu=0.95)
         # momentum: one fp32 FMA per element
         assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
         check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16 if path == "tensor" else TOL_FP32)
@@ -307,6 +308,26 @@ def test_step_weight_reduce_add_is_one_rounding_of_w_plus_update(T, H, W):
     assert torch.equal(Wa, want)
     Wn, _, _ = oracle.himuon_step(np.zeros((H, W)), f64(G), f64(M0), T, 5, lr=0.02, mu=0.95)
     check_update(f64(Wz), np.zeros((H, W)), Wn, TOL_BF16)
+
+
+@pytest.mark.parametrize("T", [64, 128])
+def test_step_mixed_weight_update_paths(T):
+    """Weights updated three ways in one call: aligned bf16 rows by TMA
+    reduce-add, unaligned rows (odd widths) and fp32 weights by the row pass,
+    wide edge tiles by the epilogue threads. Odd tile counts at T = 64 put tiles
+    of different paths into one stacked stage."""
+    shapes = [(192, 320), (130, 203), (64, 64), (200, 530), (70, 300)]
+    dtypes = [torch.bfloat16, torch.bfloat16, torch.float32, torch.bfloat16, torch.float32]
+    Ws = [torch.zeros(H, W, dtype=dt).cuda() if dt == torch.bfloat16 else
+          synth.gaussian(H, W, 7 + i, std=0.02).cuda() for i, ((H, W), dt) in enumerate(zip(shapes, dtypes))]
+    Gs = [synth.lowrank_noise(H, W, seed=150 + i).cuda() for i, (H, W) in enumerate(shapes)]
+    Ms = [synth.gaussian(H, W, 160 + i, std=1e-3).cuda() for i, (H, W) in enumerate(shapes)]
+    W0, M0 = [f64(w) for w in Ws], [f64(m) for m in Ms]
+    hm.step(Ws, Gs, Ms, T, 5, lr=0.02, mu=0.95, path="tensor")
+    for i in range(len(shapes)):
+        Wn, Mn, _ = oracle.himuon_step(W0[i], f64(Gs[i]), M0[i], T, 5, lr=0.02, mu=0.95)
+        assert rel_fro(f64(Ms[i]), Mn) <= 1e-6
+        check_update(f64(Ws[i]), W0[i], Wn, TOL_BF16)
 
 
 def test_step_zero_lr_keeps_weights_and_updates_momentum():

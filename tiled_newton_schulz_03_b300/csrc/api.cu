@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -124,12 +125,20 @@ struct himuon_handle {
   uint64_t wait_ns = 2000000000ull;
   int64_t launches = 0;        // kernels launched through this handle
   std::vector<unsigned char> host;
+  // The bytes the device workspace holds since the last upload: a call whose
+  // plan (descriptors, offsets, tensor maps) is byte-identical -- the same
+  // matrices step after step -- skips the upload. Kernels only write fields
+  // that every launch recomputes (per-matrix norm factors, norm partials).
+  std::vector<unsigned char> ws_image;
+  // Encoded tensor maps by (address, shape, leading dimension, type, box).
+  std::map<std::array<int64_t, 7>, CUtensorMap> map_cache;
 };
 
 namespace {
 
 himuon_status grow(void** buf, size_t* have, size_t need, cudaStream_t stream, const char* what) {
   if (need <= *have) return HIMUON_OK;
+  // (a new workspace holds nothing: callers that track its contents reset them)
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "workspace growth: stream sync");
   const size_t n = std::max(need, *have + *have / 2);
@@ -183,6 +192,22 @@ bool make_map(CUtensorMap* m, const void* base, int64_t H, int64_t W, int64_t ld
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// make_map through the handle's cache of encoded maps.
+bool cached_map(himuon_handle* h, CUtensorMap* m, const void* base, int64_t H, int64_t W,
+                int64_t ld, bool fp32, int box_w, int box_h) {
+  const std::array<int64_t, 7> key{static_cast<int64_t>(reinterpret_cast<uintptr_t>(base)), H, W,
+                                   ld, fp32 ? 1 : 0, box_w, box_h};
+  auto it = h->map_cache.find(key);
+  if (it != h->map_cache.end()) {
+    *m = it->second;
+    return true;
+  }
+  if (!make_map(m, base, H, W, ld, fp32, box_w, box_h)) return false;
+  if (h->map_cache.size() >= 65536) h->map_cache.clear();
+  h->map_cache.emplace(key, *m);
+  return true;
 }
 
 }  // namespace
@@ -335,11 +360,11 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
     bool ok = (d.flags & F_IN_VEC) != 0 && T >= 64;
     if (st.enabled) ok = ok && !in32 && (d.flags & F_M_VEC) && !(d.flags & F_M_BF16);
     std::memset(&maps[3 * i], 0, 3 * sizeof(CUtensorMap));
-    if (ok) ok = make_map(&maps[3 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
-    if (ok && st.enabled) ok = make_map(&maps[3 * i + 1], d.mom, d.H, d.W, d.ld_mom, true, 32, T);
+    if (ok) ok = cached_map(h, &maps[3 * i], d.in, d.H, d.W, d.ld_in, in32, in32 ? 32 : 64, T);
+    if (ok && st.enabled) ok = cached_map(h, &maps[3 * i + 1], d.mom, d.H, d.W, d.ld_mom, true, 32, T);
     if (ok) d.flags |= F_TMA;
     if (st.enabled && st.wd_factor == 1.f && !(d.flags & F_OUT_FP32) && (d.flags & F_OUT_VEC) &&
-        make_map(&maps[3 * i + 2], d.out, d.H, d.W, d.ld_out, false, 64, T))
+        cached_map(h, &maps[3 * i + 2], d.out, d.H, d.W, d.ld_out, false, 64, T))
       d.flags |= F_W_TMA;
   }
 
@@ -354,8 +379,13 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   const size_t off_maps = (off_part + sizeof(int64_t) * (n + 1) + 255) & ~size_t(255);
   const size_t off_partials = (off_maps + sizeof(CUtensorMap) * maps.size() + 255) & ~size_t(255);
   const size_t ws_need = off_partials + sizeof(float) * std::max<int64_t>(nparts, 1);
+  const void* ws_before = h->ws;
   himuon_status s = grow(&h->ws, &h->ws_bytes, ws_need, stream, "workspace");
-  if (s != HIMUON_OK) return s;
+  if (s != HIMUON_OK) {
+    h->ws_image.clear();
+    return s;
+  }
+  if (h->ws != ws_before) h->ws_image.clear();
   h->host.assign(off_partials, 0);
   std::memcpy(h->host.data() + off_desc, descs.data(), sizeof(MatDesc) * n);
   std::memcpy(h->host.data() + off_part, part_start.data(), sizeof(int64_t) * (n + 1));
@@ -364,8 +394,15 @@ himuon_status run_plan(himuon_handle* h, std::vector<MatDesc>& descs, int32_t T,
   unsigned char* ws = static_cast<unsigned char*>(h->ws);
   // Pageable source: the copy is staged before cudaMemcpyAsync returns, so the
   // host buffer may be reused by the next call right away.
-  cudaError_t e = cudaMemcpyAsync(ws, h->host.data(), off_partials, cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+  cudaError_t e = cudaSuccess;
+  if (h->ws_image != h->host) {
+    e = cudaMemcpyAsync(ws, h->host.data(), off_partials, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+      h->ws_image.clear();
+      return cuda_fail(e, "descriptor upload");
+    }
+    h->ws_image = h->host;
+  }
   MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + off_desc);
   const int64_t* d_part = reinterpret_cast<const int64_t*>(ws + off_part);
   const void* d_maps = ws + off_maps;

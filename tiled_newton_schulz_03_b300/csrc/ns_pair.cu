@@ -182,7 +182,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   // tensor memory) -> product p. CTA 0's issuer waits for CTA 1's arrival.
   auto hand_over = [&](bool tmem_written, int p) {
     if (tmem_written) ptx::tmem_wait_st();
-    ptx::fence_proxy_async_all();
+    // E3 also wrote the peer's shared memory; E1 and E2 only this CTA's
+    if (p == 0) ptx::fence_proxy_async_cluster();
+    else ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
     if (c == 1) {
@@ -215,60 +217,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int xh = tr ? w : h, xw = tr ? h : w;
     const bool in32 = d.flags & F_IN_FP32, out32 = d.flags & F_OUT_FP32;
     const bool m16 = d.flags & F_M_BF16;
-    const int ies = in32 ? 4 : 2, oes = out32 ? 4 : 2, mes = m16 ? 2 : 4;
 
     // ---- prologue: U (momentum applied for a step, M written back) into
     // R_X = a U - e U_bf and the X_bf buffers; sums of squares
     float ssq = 0.f;
     {
       const StepCoef cf0 = step_coef(ns, 0);
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        const int xc = xc0 + 32 * ch;
-        const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
-        float u[32];
-        if (!tr) {
-          const char* gp = gptr(d.in, d.ld_in, i0 + xr, j0, in32);
-          const bool vin = (d.flags & F_IN_VEC) && ((j0 + xc) * ies) % 16 == 0;
-          gload32(gp, xc, n, in32, vin, u);
-          if (STEP) {
-            char* mp = gptr(d.mom, d.ld_mom, i0 + xr, j0, !m16);
-            const bool vm = (d.flags & F_M_VEC) && ((j0 + xc) * mes) % 16 == 0;
-            float mv[32];
-            gload32(mp, xc, n, !m16, vm, mv);
-            const uint64_t mu2 = pk2(st.mu, st.mu);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const uint64_t mn = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(u[j], u[j + 1]));
-              upk2(mn, mv[j], mv[j + 1]);
-              if (st.nesterov) upk2(fma2(mu2, mn, pk2(u[j], u[j + 1])), u[j], u[j + 1]);
-              else upk2(mn, u[j], u[j + 1]);
-            }
-            if (n > 0) gstore32(mp, xc, n, !m16, vm, mv);
-          }
-        } else {
-          // X = tile^T: element (xr, xc + j) is G[i0 + xc + j][j0 + xr]; the
-          // lanes of a warp read consecutive columns of one row
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float x = 0.f;
-            if (j < n) {
-              const char* gp = gptr(d.in, d.ld_in, i0 + xc + j, j0 + xr, in32);
-              x = in32 ? *reinterpret_cast<const float*>(gp)
-                       : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(gp));
-              if (STEP) {
-                char* mp = gptr(d.mom, d.ld_mom, i0 + xc + j, j0 + xr, !m16);
-                const float m = m16 ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(mp))
-                                    : *reinterpret_cast<const float*>(mp);
-                const float mn = fmaf(st.mu, m, x);
-                if (m16) *reinterpret_cast<__nv_bfloat16*>(mp) = __float2bfloat16_rn(mn);
-                else *reinterpret_cast<float*>(mp) = mn;
-                x = st.nesterov ? fmaf(st.mu, mn, x) : mn;
-              }
-            }
-            u[j] = x;
-          }
-        }
+      // 32 values of U at this thread's row, tile columns [xc, xc + 32)
+      auto consume = [&](int xc, float (&u)[32]) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) ssq = fmaf(u[j], u[j], ssq);
         uint32_t pkd[16];
@@ -295,6 +251,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           upk2(x, u[2 * j], u[2 * j + 1]);
         }
         ptx::tmem_st32(t_x + xc, u);
+      };
+      if (!tr) {
+        // one 128-column half at a time through sC (fp32): warp w reads rows
+        // [8 w, 8 w + 8) of the CTA's 128 with its lanes along the columns (an
+        // access touches one or two cache lines whatever the alignment), applies
+        // momentum, stages U; then each thread takes its own row's 64 columns
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll 1
+          for (int i = 0; i < 8; i += 4) {
+            float gv[4][4], mv[4][4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = 128 * static_cast<int>(c) + 8 * warp + i + rr;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = 128 * h2 + lane + 32 * j;
+                const bool ok = row < xh && col < xw;
+                const int64_t gi = static_cast<int64_t>(i0 + row) * d.ld_in + j0 + col;
+                const int64_t mo = static_cast<int64_t>(i0 + row) * d.ld_mom + j0 + col;
+                gv[rr][j] = ok ? ld_val(d.in, gi, in32) : 0.f;
+                mv[rr][j] = (STEP && ok) ? ld_val(d.mom, mo, !m16) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = 128 * static_cast<int>(c) + 8 * warp + i + rr;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = 128 * h2 + lane + 32 * j;
+                float u = gv[rr][j];
+                if (STEP) {
+                  const float mn = fmaf(st.mu, mv[rr][j], u);
+                  if (row < xh && col < xw)
+                    st_val(d.mom, static_cast<int64_t>(i0 + row) * d.ld_mom + j0 + col, !m16, mn);
+                  u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
+                }
+                f32_put(sc, 8 * warp + i + rr, lane + 32 * j, u);
+              }
+            }
+          }
+          named_sync(BAR_LINK, NTHREADS);
+          if ((cq >> 1) == h2) {
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch) {
+              const int xc = xc0 + 32 * ch;
+              float u[32];
+              ld_f32_32(sc, r, xc - 128 * h2, u);
+              consume(xc, u);
+            }
+          }
+          named_sync(BAR_LINK, NTHREADS);            // sC is restaged or rewritten next
+        }
+      } else {
+        // X = tile^T: element (xr, xc + j) is G[i0 + xc + j][j0 + xr]; the
+        // lanes of a warp read consecutive columns of one row
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
+          float u[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float x = 0.f;
+            if (j < n) {
+              const int64_t gi = static_cast<int64_t>(i0 + xc + j) * d.ld_in + j0 + xr;
+              x = ld_val(d.in, gi, in32);
+              if (STEP) {
+                const int64_t mo = static_cast<int64_t>(i0 + xc + j) * d.ld_mom + j0 + xr;
+                const float mn = fmaf(st.mu, ld_val(d.mom, mo, !m16), x);
+                st_val(d.mom, mo, !m16, mn);
+                x = st.nesterov ? fmaf(st.mu, mn, x) : mn;
+              }
+            }
+            u[j] = x;
+          }
+          consume(xc, u);
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
@@ -321,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
     }
     ptx::tmem_wait_st();
-    ptx::fence_proxy_async_all();
+    ptx::fence_proxy_async_cluster();
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
     // tile norm: each CTA's sum (fixed order) goes to the peer, with an arrival
@@ -378,8 +412,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           for (int ch = 0; ch < 2; ++ch) {
             const int xc = xc0 + 32 * ch;
             float v[32], av[32];
+            ld_bf16_32(sc, r, xc, av);               // in flight during the TMEM load
             ptx::tmem_ld32_sync(t_a + xc, v);
-            ld_bf16_32(sc, r, xc, av);
             const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -436,39 +470,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             ptx::tmem_st32(t_x + xc, v);
             continue;
           }
-          // last step: out = X' (NS map), or W <- wd W - lr s X' (step)
+          // last step. A transposed tile: out = X'^T (NS map), or W <- wd W -
+          // lr s X'^T (step), the lanes writing consecutive columns of one row.
+          if (!tr) {                                 // staged one half at a time below:
+            if ((cq >> 1) == 0) st_f32_32(sc, r, xc & 127, v);   // the first half now
+            continue;
+          }
           const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
-          if (n == 0) continue;
-          if (!tr) {
-            char* op = gptr(d.out, d.ld_out, i0 + xr, j0, out32);
-            const bool vo = (d.flags & F_OUT_VEC) && ((j0 + xc) * oes) % 16 == 0;
-            if (STEP) {
-              float wv[32];
-              gload32(op, xc, n, out32, vo, wv);
-              const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale), wdf = pk2(st.wd_factor, st.wd_factor);
 #pragma unroll
-              for (int j = 0; j < 32; j += 2)
-                upk2(fma2(nls, pk2(v[j], v[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1]))), wv[j], wv[j + 1]);
-              gstore32(op, xc, n, out32, vo, wv);
-            } else {
-              gstore32(op, xc, n, out32, vo, v);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j >= n) break;
-              char* op = gptr(d.out, d.ld_out, i0 + xc + j, j0 + xr, out32);
-              float o = v[j];
-              if (STEP) {
-                const float wv = out32 ? *reinterpret_cast<const float*>(op)
-                                       : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(op));
-                o = fmaf(-d.upd_scale, o, wv * st.wd_factor);
+          for (int j = 0; j < 32; ++j) {
+            if (j >= n) break;
+            const int64_t oi = static_cast<int64_t>(i0 + xc + j) * d.ld_out + j0 + xr;
+            float o = v[j];
+            if (STEP) o = fmaf(-d.upd_scale, o, ld_val(d.out, oi, out32) * st.wd_factor);
+            st_val(d.out, oi, out32, o);
+          }
+        }
+      }
+      if (last && !tr) {
+        // last step, the tile as it is: X' goes through sC (fp32) one
+        // 128-column half at a time (the half held by column quarters 2 h2 and
+        // 2 h2 + 1 was staged above for h2 = 0); warp w then writes rows
+        // [8 w, 8 w + 8) of the CTA's 128 with its lanes along the columns:
+        // out = X' (NS map), or W <- wd W - lr s X' (step)
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (h2 == 1) {
+            named_sync(BAR_LINK, NTHREADS);          // the first half has been written out
+            if ((cq >> 1) == 1) {
+#pragma unroll 1
+              for (int ch = 0; ch < 2; ++ch) {
+                const int xc = xc0 + 32 * ch;
+                float v[32];
+                ptx::tmem_ld32_sync(t_x + xc, v);
+                if (K == 1) scale32(v, sc_t);
+                st_f32_32(sc, r, xc & 127, v);
               }
-              if (out32) *reinterpret_cast<float*>(op) = o;
-              else *reinterpret_cast<__nv_bfloat16*>(op) = __float2bfloat16_rn(o);
+            }
+          }
+          named_sync(BAR_LINK, NTHREADS);
+#pragma unroll 1
+          for (int i = 0; i < 8; i += 4) {
+            float wv[4][4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = 128 * static_cast<int>(c) + 8 * warp + i + rr;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = 128 * h2 + lane + 32 * j;
+                const int64_t oi = static_cast<int64_t>(i0 + row) * d.ld_out + j0 + col;
+                wv[rr][j] = (STEP && row < xh && col < xw) ? ld_val(d.out, oi, out32) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int row = 128 * static_cast<int>(c) + 8 * warp + i + rr;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = 128 * h2 + lane + 32 * j;
+                if (row >= xh || col >= xw) continue;
+                const int64_t oi = static_cast<int64_t>(i0 + row) * d.ld_out + j0 + col;
+                float o = f32_at(sc, 8 * warp + i + rr, lane + 32 * j);
+                if (STEP) o = fmaf(-d.upd_scale, o, wv[rr][j] * st.wd_factor);
+                st_val(d.out, oi, out32, o);
+              }
             }
           }
         }
+        named_sync(BAR_LINK, NTHREADS);              // sC is free for the next tile
       }
       if (!last) hand_over(true, 0);       // -> next X X^T
     }

@@ -86,9 +86,11 @@ struct Ctl {
   float info_s[4];
   int ticket;             // next stage to hand to a free slot
   int ticket_s[2];        // the stage each slot took
-  // per slot and stacked tile: where its -lr s O goes by TMA reduce-add
-  // (matrix or -1, origin, width); copied from info_* when the slot takes a stage
-  int red_mi[2][2], red_i0[2][2], red_j0[2][2], red_w[2][2];
+  // per slot and stacked tile, copied from info_* when the slot takes a stage:
+  // how the step's weight update is written (fin_mode: 0 by the epilogue
+  // threads, 1 TMA reduce-add of -lr s O, 2 row pass from sC), matrix, origin
+  // and extent
+  int fin_mode[2][2], fin_mi[2][2], fin_i0[2][2], fin_j0[2][2], fin_h[2][2], fin_w[2][2];
 };
 
 // Tile of a launch's flat list: matrix, origin and valid extent.
@@ -115,6 +117,46 @@ __device__ __forceinline__ int tile_format(int flags) {
   return (flags & F_IN_FP32) ? FMT_U32 : FMT_G16;
 }
 
+// Weight update of the stage's row-pass tiles from O staged in sC (fp32, the
+// swizzled layout of 4-column chunks, stage rows x 64 columns starting at tile
+// column col0): W <- wd W - lr s O. Warp ws of the slot takes stage rows
+// [16 ws, 16 ws + 16), four at a time; lane l takes columns l and l + 32.
+template <int T>
+__device__ __forceinline__ void w_row_pass(const Ctl& ctl, int s, const MatDesc* descs, uint32_t sc,
+                                           int col0, int ws, int lane, float wd_factor) {
+#pragma unroll 1
+  for (int r0 = 16 * ws; r0 < 16 * ws + 16; r0 += 4) {
+    float wv[4][2];
+    int64_t idx[4][2];
+    bool ok[4][2];
+    const MatDesc* d[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = r0 + rr, u = r / T, rl = r % T;
+      const bool row = ctl.fin_mode[s][u] == 2 && rl < ctl.fin_h[s][u];
+      d[rr] = &descs[row ? ctl.fin_mi[s][u] : 0];
+      const bool out32 = d[rr]->flags & F_OUT_FP32;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = col0 + lane + 32 * q;
+        ok[rr][q] = row && c < ctl.fin_w[s][u];
+        idx[rr][q] = static_cast<int64_t>(ctl.fin_i0[s][u] + rl) * d[rr]->ld_out + ctl.fin_j0[s][u] + c;
+        wv[rr][q] = ok[rr][q] ? ld_val(d[rr]->out, idx[rr][q], out32) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const bool out32 = d[rr]->flags & F_OUT_FP32;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (!ok[rr][q]) continue;
+        const float o = f32_at(sc, r0 + rr, lane + 32 * q);
+        st_val(d[rr]->out, idx[rr][q], out32, fmaf(-d[rr]->upd_scale, o, wv[rr][q] * wd_factor));
+      }
+    }
+  }
+}
+
 // One thread adds the stage's -lr s O tiles (bf16, in the slot's sC buffer, the
 // swizzled layout of the TMA box) to W by TMA reduce-add, one box of 64
 // columns x T rows per 64 valid columns. Returns whether a bulk group was
@@ -125,14 +167,13 @@ __device__ __noinline__ bool issue_w_reduce(const Ctl& ctl, int s, const CUtenso
   constexpr int TPS = 128 / T;
   bool any = false;
   for (int u = 0; u < TPS; ++u) {
-    const int m_u = ctl.red_mi[s][u];
-    if (m_u < 0) continue;
-    const CUtensorMap* mw = maps + 3 * m_u + 2;
+    if (ctl.fin_mode[s][u] != 1) continue;
+    const CUtensorMap* mw = maps + 3 * ctl.fin_mi[s][u] + 2;
     tensormap_acquire(mw);
     for (int b = 0; b < T / 64; ++b) {
-      if (64 * b >= ctl.red_w[s][u]) break;            // box wholly right of the matrix
-      ptx::tma_reduce_add_2d(mw, sc + b * 16384 + u * T * 128, ctl.red_j0[s][u] + 64 * b,
-                             ctl.red_i0[s][u]);
+      if (64 * b >= ctl.fin_w[s][u]) break;            // box wholly right of the matrix
+      ptx::tma_reduce_add_2d(mw, sc + b * 16384 + u * T * 128, ctl.fin_j0[s][u] + 64 * b,
+                             ctl.fin_i0[s][u]);
     }
     any = true;
   }
@@ -195,7 +236,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp < 4) {
     // =============================================================== loader
     const int r = threadIdx.x;              // stage row
-    const int t = r / T, rl = r % T;        // sub-tile and row within it
     int last_mi = -1;
     uint32_t ld_phase = 0;
     // TMA-staged momentum of the stage last handed to a slot: the slot writes
@@ -295,37 +335,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
       // ---- rows TMA does not bring: plain loads (any alignment) into the fp32
       // tile as U, momentum applied and M written back here; zeros for a stage's
-      // missing tiles.
-      const TileRef& me = ref[t];
-      if (me.mi < 0) {
-        float z[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0.f;
-        for (int c = 0; c < T; c += 32) st_f32_32(sbase + SM_S0, r, c, z);
-      } else if (!(descs[me.mi].flags & F_TMA)) {
-        const MatDesc& d = descs[me.mi];
-        const bool in32 = d.flags & F_IN_FP32;
-        const bool row_ok = rl < me.h;
-        const char* gp = row_ok ? gptr(d.in, d.ld_in, me.i0 + rl, me.j0, in32) : nullptr;
-        const bool m16 = d.flags & F_M_BF16;
-        char* mp = (STEP && row_ok) ? gptr(d.mom, d.ld_mom, me.i0 + rl, me.j0, !m16) : nullptr;
+      // missing tiles. A warp takes 32 stage rows (all in one tile, since
+      // T >= 64) and reads each row with its lanes along the columns, four rows
+      // in flight, so that an instruction touches one or two cache lines
+      // whatever the alignment of the rows.
+      {
+        const int ln = r & 31;
+        const int r0 = r & ~31;                  // first stage row of this warp
+        const TileRef& me = ref[r0 / T];
+        const int rl0 = r0 % T;                  // its row within the tile
+        constexpr int NJ = T / 32;               // columns per lane
+        if (me.mi < 0) {
 #pragma unroll 1
-        for (int c = 0; c < T; c += 32) {
-          const int n = row_ok ? max(0, min(32, me.w - c)) : 0;
-          float u[32];
-          gload32(gp, c, n, in32, d.flags & F_IN_VEC, u);
-          if (STEP) {
-            float mv[32];
-            gload32(mp, c, n, !m16, d.flags & F_M_VEC, mv);
+          for (int i = 0; i < 32; ++i)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float mn = fmaf(st.mu, mv[j], u[j]);
-              mv[j] = mn;
-              u[j] = st.nesterov ? fmaf(st.mu, mn, u[j]) : mn;
+            for (int j = 0; j < NJ; ++j) f32_put(sbase + SM_S0, r0 + i, ln + 32 * j, 0.f);
+        } else if (!(descs[me.mi].flags & F_TMA)) {
+          const MatDesc& d = descs[me.mi];
+          const bool in32 = d.flags & F_IN_FP32, m32 = !(d.flags & F_M_BF16);
+#pragma unroll 1
+          for (int i = 0; i < 32; i += 4) {
+            float gv[4][NJ], mv[4][NJ];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int rl = rl0 + i + rr;
+#pragma unroll
+              for (int j = 0; j < NJ; ++j) {
+                const int c = ln + 32 * j;
+                const bool ok = rl < me.h && c < me.w;
+                gv[rr][j] = ok ? ld_val(d.in, static_cast<int64_t>(me.i0 + rl) * d.ld_in + me.j0 + c, in32) : 0.f;
+                mv[rr][j] = (STEP && ok) ? ld_val(d.mom, static_cast<int64_t>(me.i0 + rl) * d.ld_mom + me.j0 + c, m32) : 0.f;
+              }
             }
-            if (n > 0) gstore32(mp, c, n, !m16, d.flags & F_M_VEC, mv);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int rl = rl0 + i + rr;
+#pragma unroll
+              for (int j = 0; j < NJ; ++j) {
+                const int c = ln + 32 * j;
+                float u = gv[rr][j];
+                if (STEP) {
+                  const float mn = fmaf(st.mu, mv[rr][j], u);
+                  if (rl < me.h && c < me.w)
+                    st_val(d.mom, static_cast<int64_t>(me.i0 + rl) * d.ld_mom + me.j0 + c, m32, mn);
+                  u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
+                }
+                f32_put(sbase + SM_S0, r0 + i + rr, c, u);
+              }
+            }
           }
-          st_f32_32(sbase + SM_S0, r, c, u);
         }
       }
       if (any_tma) {
@@ -556,17 +614,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int th = ctl.info_h[t], tw = ctl.info_w[t];
       const int fmt = ctl.info_fmt[t];
       const float s_info = ctl.info_s[t];
-      // the stage's tiles whose weights take the TMA reduce-add, copied now: the
+      // how each tile of the stage writes its weight update, copied now: the
       // loader rewrites ctl.info_* for the next stage once staging is released
       if (STEP && issuer) {
 #pragma unroll
         for (int u = 0; u < TPS; ++u) {
           const int m_u = ctl.info_mi[u];
-          const bool ok = m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u] && (descs[m_u].flags & F_W_TMA);
-          ctl.red_mi[s][u] = ok ? m_u : -1;
-          ctl.red_i0[s][u] = ctl.info_i0[u];
-          ctl.red_j0[s][u] = ctl.info_j0[u];
-          ctl.red_w[s][u] = ctl.info_w[u];
+          int mode = 0;                    // transposed tiles: by the epilogue threads
+          if (m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u])
+            mode = (descs[m_u].flags & F_W_TMA) ? 1 : 2;
+          ctl.fin_mode[s][u] = mode;
+          ctl.fin_mi[s][u] = m_u;
+          ctl.fin_i0[s][u] = ctl.info_i0[u];
+          ctl.fin_j0[s][u] = ctl.info_j0[u];
+          ctl.fin_h[s][u] = ctl.info_h[u];
+          ctl.fin_w[s][u] = ctl.info_w[u];
         }
       }
 
@@ -694,8 +756,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int ch = 0; ch < nch; ++ch) {
             const int c = cbase + 32 * ch;
             float v[32], av[32];
+            ld_bf16_32(sc, r, c, av);                // in flight during the TMEM load
             ptx::tmem_ld32_sync(t_a + c, v);
-            ld_bf16_32(sc, r, c, av);
             const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -717,8 +779,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         wait_acc();
         const bool last = (k + 1 == K);
         const StepCoef cfn = step_coef(ns, last ? k : k + 1);
-        // step: W += -lr s O by a TMA reduce-add from sC (bf16 W, no decay)
+        // step: W += -lr s O by a TMA reduce-add from sC (bf16 W, no decay), or
+        // O staged in sC (fp32, 64 columns at a time) for a row pass
         const bool w_red = STEP && last && mi >= 0 && !tr && (descs[mi].flags & F_W_TMA);
+        const bool w_rows = STEP && last && mi >= 0 && !tr && !w_red;
 #pragma unroll 1
         for (int ch = 0; ch < nch; ++ch) {
           const int c = cbase + 32 * ch;
@@ -730,6 +794,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               scale32(v, -descs[mi].upd_scale);     // -lr s O, added to W by TMA below
               uint32_t pkd[16];
               st_bf16_32(sc, r, c, v, pkd);
+            } else if (w_rows) {
+              if (c < 64) st_f32_32(sc, r, c, v);   // columns [64, 128) in a second round
             } else if (mi >= 0) {
               emit(descs[mi], i0, j0, th, tw, tr, c, v);
             }
@@ -753,6 +819,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::fence_proxy_async_smem();
         named_sync(2 + s, SLOT_THREADS);
         if (issuer && !*abort_flag && issue_w_reduce<T>(ctl, s, maps, sc)) reduce_pending = true;
+        // tiles whose W is read and written here (unaligned rows, fp32 W, weight
+        // decay): O is in sC (fp32, 64 columns); the slot's warps update W row by
+        // row with the lanes along the columns, so that an access touches one or
+        // two cache lines whatever the alignment; T = 128 takes two rounds
+        bool any_rows = false;
+#pragma unroll
+        for (int u = 0; u < TPS; ++u) any_rows |= ctl.fin_mode[s][u] == 2;
+        if (any_rows) {
+          w_row_pass<T>(ctl, s, descs, sc, 0, ws, lane, st.wd_factor);
+          if (T == 128) {
+            named_sync(2 + s, SLOT_THREADS);        // round 0 has read sC
+            if (mi >= 0 && !tr && !(descs[mi].flags & F_W_TMA) && cbase >= 64) {
+#pragma unroll 1
+              for (int ch = 0; ch < nch; ++ch) {
+                const int c = cbase + 32 * ch;
+                float v[32];
+                ptx::tmem_ld32_sync(t_x + c, v);
+                if (K == 1) scale32(v, sc_t);
+                st_f32_32(sc, r, c - 64, v);
+              }
+            }
+            named_sync(2 + s, SLOT_THREADS);
+            w_row_pass<T>(ctl, s, descs, sc, 64, ws, lane, st.wd_factor);
+          }
+        }
       }
     }
     if (reduce_pending) ptx::bulk_wait0();     // the reduces have completed before exit

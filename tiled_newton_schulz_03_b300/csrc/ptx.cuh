@@ -267,9 +267,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Generic-proxy writes (local or remote shared memory) made visible to the async proxy.
-__device__ __forceinline__ void fence_proxy_async_all() {
-  asm volatile("fence.proxy.async;" ::: "memory");
+// Generic-proxy writes to shared memory of any CTA of the cluster (this CTA's
+// included) made visible to the async proxy.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // All threads of every CTA of the cluster.

@@ -172,6 +172,16 @@ __device__ __forceinline__ void gstore32(void* rowp, int c0, int n, bool fp32, b
   }
 }
 
+// one element of a bf16 or fp32 matrix, as fp32 (and back, rounded to nearest)
+__device__ __forceinline__ float ld_val(const void* base, int64_t idx, bool fp32) {
+  return fp32 ? static_cast<const float*>(base)[idx]
+              : __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+}
+__device__ __forceinline__ void st_val(void* base, int64_t idx, bool fp32, float v) {
+  if (fp32) static_cast<float*>(base)[idx] = v;
+  else static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+}
+
 __device__ __forceinline__ char* gptr(const void* base, int64_t ld, int64_t row, int64_t col,
                                       bool fp32) {
   return const_cast<char*>(static_cast<const char*>(base)) + (row * ld + col) * (fp32 ? 4 : 2);
