@@ -336,6 +336,17 @@ def run_ours(args):
         hm.step(Ws, Gs, Ms, T, K, lr=0.02, mu=0.95, nesterov=True, chunk_bytes=chunk,
                 handle=handle, stream=stream)
 
+    if args.mode == "sharded":
+        # strong scaling: each rank steps the matrices it owns (balanced by NS
+        # work) and the owners broadcast the new weights to every rank
+        from tiled_newton_schulz_03_b300 import shard
+        sharded = shard.ShardedStep(shapes, T, K, lambda W, G, M: hm.step(
+            W, G, M, T, K, lr=0.02, mu=0.95, nesterov=True, chunk_bytes=chunk, handle=handle,
+            stream=stream))
+
+        def one_step():                       # noqa: F811
+            sharded(Ws, Gs, Ms)
+
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
@@ -360,7 +371,8 @@ def run_ours(args):
     if hm.device_error(handle=handle) != 0:
         raise RuntimeError("device error during the timed region")
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    jobs = 1 if args.mode == "sharded" else world   # layer sets stepped per step, all ranks
+    value = jobs * flops * args.steps / (total_ms * 1e-3) / 1e12
 
     # Roofline of the fused step kernel. Its launches run back to back on the
     # stream and are the whole step (ncu launch list), so the average launch
@@ -391,7 +403,7 @@ def run_ours(args):
 
     # end to end through the public API: G from pinned host memory, step, W back
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.mode == "replicas":
         e2e = run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, world, dev)
 
     cpu = None
@@ -411,7 +423,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong" if args.mode == "sharded" else "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded low-rank + noise gradients, N(0,0.02^2) weights, zero momentum)",
         "config": {"workload": f"{args.workload}: {len(shapes)} matrices, {nparams / 1e9:.2f} G params, "
                                f"T={T}, K={K}, fused momentum(0.95, Nesterov) + update(lr 0.02)",
@@ -419,7 +432,7 @@ def run_ours(args):
                    "chunk_bytes": chunk, "grad_dtype": "bf16", "weight_dtype": "bf16",
                    "momentum_dtype": "fp32", "l2": "inputs larger than L2 (G+M+W = "
                    f"{nbytes / 1e9:.0f} GB per step)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": (f"{args.mode} x{world}" if world > 1 else "single GPU")},
         "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
                     "max": round(max(step_ms), 3)},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -731,6 +744,9 @@ def main():
                     default="llama3_8b",
                     help="llama3_8b (headline) or gpt2_small: the fused step, one JSON line; "
                          "sweep4096 / ragged: the secondary entries alone, one line each")
+    ap.add_argument("--mode", choices=["replicas", "sharded"], default="replicas",
+                    help="N > 1: replicas (every rank steps the whole layer set; weak scaling) or "
+                         "sharded (each rank steps its share, owners broadcast W; strong scaling)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -141,11 +141,13 @@ void himuon_default_ns_params(himuon_ns_params* p);
  * Tiled NS map of one matrix (abstract, sentences 3-5).
  * G: H x W input, ld ldg, dtype gtype (BF16 or FP32).
  * out: H x W output, ld ldo, dtype otype (BF16 or FP32); may be G itself.
- * T: tile size, 1 <= T. The tensor path runs T <= 32 one tile per warp
- *    (warp-level MMA), T = 64 and 128 on chip (tcgen05), and every T >= 65
- *    (including 256, and T >= max(H, W): one tile = the full-matrix map of
- *    Muon, sentences 1-2) as batched GEMMs; 32 < T < 64 returns
- *    HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any T.
+ * T: tile size, 1 <= T. The tensor path keeps every tile on chip for all K
+ *    steps for T <= 32 (one tile per warp, warp-level MMA), T = 64 and 128
+ *    (one SM, tcgen05) and 128 < T <= 256 (one tile on a pair of SMs,
+ *    tcgen05 cta_group::2); every other T >= 65 (and T >= max(H, W): one tile
+ *    = the full-matrix map of Muon, sentences 1-2) runs as batched GEMMs;
+ *    32 < T < 64 returns HIMUON_ERR_UNSUPPORTED there. The fp32 path takes any
+ *    T.
  * K: number of NS steps, 0 <= K <= 64.
  * params: NULL means the defaults.
  * Returns HIMUON_ERR_INVALID_ARG for H or W < 1, ld < W, NULL pointers, bad

@@ -217,6 +217,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int xh = tr ? w : h, xw = tr ? h : w;
     const bool in32 = d.flags & F_IN_FP32, out32 = d.flags & F_OUT_FP32;
     const bool m16 = d.flags & F_M_BF16;
+    // output (or W) rows that allow 16-byte accesses: written by each thread
+    // from its own row segment; otherwise staged and written coalesced by warps
+    const bool vec_out = (d.flags & F_OUT_VEC) && (j0 * (out32 ? 4 : 2)) % 16 == 0;
 
     // ---- prologue: U (momentum applied for a step, M written back) into
     // R_X = a U - e U_bf and the X_bf buffers; sums of squares
@@ -252,7 +255,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         ptx::tmem_st32(t_x + xc, u);
       };
-      if (!tr) {
+      // rows that allow 16-byte accesses of G (and M): each thread reads its own
+      // row segment with vector loads; otherwise the rows are read coalesced by
+      // warps and staged through sC
+      const bool vec_rows = (d.flags & F_IN_VEC) && (j0 * (in32 ? 4 : 2)) % 16 == 0 &&
+                            (!STEP || ((d.flags & F_M_VEC) && (j0 * (m16 ? 2 : 4)) % 16 == 0));
+      if (!tr && vec_rows) {
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
+          float u[32];
+          gload32(gptr(d.in, d.ld_in, i0 + xr, j0, in32), xc, n, in32, true, u);
+          if (STEP) {
+            char* mp = gptr(d.mom, d.ld_mom, i0 + xr, j0, !m16);
+            float mv[32];
+            gload32(mp, xc, n, !m16, true, mv);
+            const uint64_t mu2 = pk2(st.mu, st.mu);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint64_t mn = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(u[j], u[j + 1]));
+              upk2(mn, mv[j], mv[j + 1]);
+              if (st.nesterov) upk2(fma2(mu2, mn, pk2(u[j], u[j + 1])), u[j], u[j + 1]);
+              else upk2(mn, u[j], u[j + 1]);
+            }
+            if (n > 0) gstore32(mp, xc, n, !m16, true, mv);
+          }
+          consume(xc, u);
+        }
+      } else if (!tr) {
         // one 128-column half at a time through sC (fp32): warp w reads rows
         // [8 w, 8 w + 8) of the CTA's 128 with its lanes along the columns (an
         // access touches one or two cache lines whatever the alignment), applies
@@ -472,6 +503,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           }
           // last step. A transposed tile: out = X'^T (NS map), or W <- wd W -
           // lr s X'^T (step), the lanes writing consecutive columns of one row.
+          if (!tr && vec_out) {                      // 16-byte stores of the own row segment
+            const int n = (xr < xh) ? max(0, min(32, xw - xc)) : 0;
+            if (n == 0) continue;
+            char* op = gptr(d.out, d.ld_out, i0 + xr, j0, out32);
+            if (STEP) {
+              float wv[32];
+              gload32(op, xc, n, out32, true, wv);
+              const uint64_t nls = pk2(-d.upd_scale, -d.upd_scale), wdf = pk2(st.wd_factor, st.wd_factor);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2)
+                upk2(fma2(nls, pk2(v[j], v[j + 1]), mul2(wdf, pk2(wv[j], wv[j + 1]))), wv[j], wv[j + 1]);
+              gstore32(op, xc, n, out32, true, wv);
+            } else {
+              gstore32(op, xc, n, out32, true, v);
+            }
+            continue;
+          }
           if (!tr) {                                 // staged one half at a time below:
             if ((cq >> 1) == 0) st_f32_32(sc, r, xc & 127, v);   // the first half now
             continue;
@@ -487,7 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (last && !tr) {
+      if (last && !tr && !vec_out) {
         // last step, the tile as it is: X' goes through sC (fp32) one
         // 128-column half at a time (the half held by column quarters 2 h2 and
         // 2 h2 + 1 was staged above for h2 = 0); warp w then writes rows

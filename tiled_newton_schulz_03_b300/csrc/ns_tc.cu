@@ -78,6 +78,7 @@ struct Ctl {
   uint64_t st_full[2];    // loader -> slots: staging holds stage g (barrier g % 2)
   uint64_t st_empty;      // slot -> loader: staging has been read
   uint64_t st_loaded;     // TMA -> loader: staging bytes have landed
+  uint64_t rows_loaded;   // bulk row copies (unaligned bf16 rows) -> loader
   uint64_t drain[2];      // slot issuer: all its MMAs complete (abort path)
   uint32_t tmem_base;
   int abort_flag;
@@ -117,11 +118,13 @@ __device__ __forceinline__ int tile_format(int flags) {
   return (flags & F_IN_FP32) ? FMT_U32 : FMT_G16;
 }
 
-// Weight update of the stage's row-pass tiles from O staged in sC (fp32, the
-// swizzled layout of 4-column chunks, stage rows x 64 columns starting at tile
-// column col0): W <- wd W - lr s O. Warp ws of the slot takes stage rows
-// [16 ws, 16 ws + 16), four at a time; lane l takes columns l and l + 32.
-template <int T>
+// Output of the stage's row-pass tiles from O staged in sC (fp32, the swizzled
+// layout of 4-column chunks, stage rows x 64 columns starting at tile column
+// col0): out = O (NS map) or W <- wd W - lr s O (step). Warp ws of the slot
+// takes stage rows [16 ws, 16 ws + 16), four at a time; lane l takes columns l
+// and l + 32, so that an access touches one or two cache lines whatever the
+// alignment of the rows.
+template <int T, bool STEP>
 __device__ __forceinline__ void w_row_pass(const Ctl& ctl, int s, const MatDesc* descs, uint32_t sc,
                                            int col0, int ws, int lane, float wd_factor) {
 #pragma unroll 1
@@ -141,7 +144,7 @@ __device__ __forceinline__ void w_row_pass(const Ctl& ctl, int s, const MatDesc*
         const int c = col0 + lane + 32 * q;
         ok[rr][q] = row && c < ctl.fin_w[s][u];
         idx[rr][q] = static_cast<int64_t>(ctl.fin_i0[s][u] + rl) * d[rr]->ld_out + ctl.fin_j0[s][u] + c;
-        wv[rr][q] = ok[rr][q] ? ld_val(d[rr]->out, idx[rr][q], out32) : 0.f;
+        wv[rr][q] = (STEP && ok[rr][q]) ? ld_val(d[rr]->out, idx[rr][q], out32) : 0.f;
       }
     }
 #pragma unroll
@@ -151,7 +154,8 @@ __device__ __forceinline__ void w_row_pass(const Ctl& ctl, int s, const MatDesc*
       for (int q = 0; q < 2; ++q) {
         if (!ok[rr][q]) continue;
         const float o = f32_at(sc, r0 + rr, lane + 32 * q);
-        st_val(d[rr]->out, idx[rr][q], out32, fmaf(-d[rr]->upd_scale, o, wv[rr][q] * wd_factor));
+        st_val(d[rr]->out, idx[rr][q], out32,
+               STEP ? fmaf(-d[rr]->upd_scale, o, wv[rr][q] * wd_factor) : o);
       }
     }
   }
@@ -204,6 +208,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t b_full[2] = {ptx::smem_u32(&ctl.st_full[0]), ptx::smem_u32(&ctl.st_full[1])};
   const uint32_t b_empty = ptx::smem_u32(&ctl.st_empty);
   const uint32_t b_loaded = ptx::smem_u32(&ctl.st_loaded);
+  const uint32_t b_rows = ptx::smem_u32(&ctl.rows_loaded);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     ptx::mbar_init(b_empty, 1);
     ptx::mbar_init(b_loaded, 1);
+    ptx::mbar_init(b_rows, LOADER_THREADS);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
     ctl.ticket = 0;
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // =============================================================== loader
     const int r = threadIdx.x;              // stage row
     int last_mi = -1;
-    uint32_t ld_phase = 0;
+    uint32_t ld_phase = 0, rows_phase = 0;
     // TMA-staged momentum of the stage last handed to a slot: the slot writes
     // M <- mu M + G into the staging buffer; once it has released the buffer,
     // thread 0 stores it to HBM and waits until the store has read it.
@@ -288,6 +294,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
 
+      // bf16 rows that TMA cannot describe are fetched by bulk row copies when
+      // the whole stage takes that path (no TMA tile in it; fp32 momentum)
+      bool rows_bulk = false;
+      {
+        bool ok = true;
+#pragma unroll
+        for (int u = 0; u < TPS; ++u) {
+          if (ref[u].mi < 0) continue;
+          const int f = descs[ref[u].mi].flags;
+          if ((f & F_TMA) || (f & F_IN_FP32) || (STEP && (f & F_M_BF16))) ok = false;
+          else rows_bulk = true;
+        }
+        rows_bulk = rows_bulk && ok;
+      }
+
       if (any_tma && r == 0 && !*abort_flag) {
         uint32_t bytes = 0;
 #pragma unroll
@@ -336,9 +357,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- rows TMA does not bring: plain loads (any alignment) into the fp32
       // tile as U, momentum applied and M written back here; zeros for a stage's
       // missing tiles. A warp takes 32 stage rows (all in one tile, since
-      // T >= 64) and reads each row with its lanes along the columns, four rows
-      // in flight, so that an instruction touches one or two cache lines
-      // whatever the alignment of the rows.
+      // T >= 64) and reads each row with its lanes along the columns, so that an
+      // instruction touches one or two cache lines whatever the alignment of the
+      // rows. fp32 momentum goes first, all 32 rows at once, by cp.async straight
+      // into the staging tile (no registers held); G follows in batches of rows
+      // held in registers while the momentum lands.
       {
         const int ln = r & 31;
         const int r0 = r & ~31;                  // first stage row of this warp
@@ -350,40 +373,151 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int i = 0; i < 32; ++i)
 #pragma unroll
             for (int j = 0; j < NJ; ++j) f32_put(sbase + SM_S0, r0 + i, ln + 32 * j, 0.f);
-        } else if (!(descs[me.mi].flags & F_TMA)) {
+        } else if (!(descs[me.mi].flags & F_TMA) && !rows_bulk) {
           const MatDesc& d = descs[me.mi];
           const bool in32 = d.flags & F_IN_FP32, m32 = !(d.flags & F_M_BF16);
+          auto m_index = [&](int rl, int c) {
+            return static_cast<int64_t>(me.i0 + rl) * d.ld_mom + me.j0 + c;
+          };
+          if (STEP && m32) {
 #pragma unroll 1
-          for (int i = 0; i < 32; i += 4) {
-            float gv[4][NJ], mv[4][NJ];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              const int rl = rl0 + i + rr;
+            for (int i = 0; i < 32; ++i) {
+              const int rl = rl0 + i;
 #pragma unroll
               for (int j = 0; j < NJ; ++j) {
                 const int c = ln + 32 * j;
                 const bool ok = rl < me.h && c < me.w;
-                gv[rr][j] = ok ? ld_val(d.in, static_cast<int64_t>(me.i0 + rl) * d.ld_in + me.j0 + c, in32) : 0.f;
-                mv[rr][j] = (STEP && ok) ? ld_val(d.mom, static_cast<int64_t>(me.i0 + rl) * d.ld_mom + me.j0 + c, m32) : 0.f;
+                const float* src = static_cast<const float*>(d.mom) + (ok ? m_index(rl, c) : 0);
+                ptx::cp_async_4(sbase + SM_S0 + f32_off(r0 + i, c >> 2) + (c & 3) * 4, src, ok ? 4u : 0u);
               }
             }
+            ptx::cp_async_commit();
+          }
+          constexpr int RB = 32 / NJ;            // rows of G per batch: 32 values per lane
+          constexpr int RM = 16 / NJ;            // rows per batch with bf16 momentum in registers
+          const bool m_regs = STEP && !m32;
+#pragma unroll 1
+          for (int i = 0; i < 32; i += (m_regs ? RM : RB)) {
+            const int nb = m_regs ? RM : RB;
+            float gv[RB][NJ], mv[RM][NJ];
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
+            for (int rr = 0; rr < RB; ++rr) {
+              const int rl = rl0 + i + rr;
+#pragma unroll
+              for (int j = 0; j < NJ; ++j) {
+                const int c = ln + 32 * j;
+                const bool ok = rr < nb && rl < me.h && c < me.w;
+                gv[rr][j] = ok ? ld_val(d.in, static_cast<int64_t>(me.i0 + rl) * d.ld_in + me.j0 + c, in32) : 0.f;
+                if (rr < RM) mv[rr][j] = (m_regs && ok) ? ld_val(d.mom, m_index(rl, c), false) : 0.f;
+              }
+            }
+            if (STEP && m32 && i == 0) {
+              ptx::cp_async_wait_all();          // this lane's momentum has landed
+              __syncwarp();
+            }
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+              if (rr >= nb) break;
               const int rl = rl0 + i + rr;
 #pragma unroll
               for (int j = 0; j < NJ; ++j) {
                 const int c = ln + 32 * j;
                 float u = gv[rr][j];
                 if (STEP) {
-                  const float mn = fmaf(st.mu, mv[rr][j], u);
-                  if (rl < me.h && c < me.w)
-                    st_val(d.mom, static_cast<int64_t>(me.i0 + rl) * d.ld_mom + me.j0 + c, m32, mn);
+                  const float m = m32 ? f32_at(sbase + SM_S0, r0 + i + rr, c) : mv[rr < RM ? rr : 0][j];
+                  const float mn = fmaf(st.mu, m, u);
+                  if (rl < me.h && c < me.w) st_val(d.mom, m_index(rl, c), m32, mn);
                   u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
                 }
                 f32_put(sbase + SM_S0, r0 + i + rr, c, u);
               }
             }
           }
+        }
+      }
+      if (rows_bulk) {
+        // Every row of G (bf16, rows not 16-byte aligned) comes in by one bulk
+        // copy of its 16-byte aligned cover (at most 15 bytes more on either
+        // side, inside the same 16-byte chunks, so always mapped memory), 64
+        // stage rows per round into SM_S1 at a stride of 2 T + 16 bytes;
+        // fp32 momentum by cp.async into the staging tile, all rows at once.
+        // The warps then read each row with the lanes along the columns,
+        // apply momentum (M written back, coalesced) and store U.
+        constexpr int ROWB = 2 * T + 16;
+        constexpr int NJ = T / 32;
+        const int ln = r & 31, wl = r >> 5;
+        auto row_src = [&](int row, const TileRef& tf) -> uintptr_t {
+          const MatDesc& d = descs[tf.mi];
+          return reinterpret_cast<uintptr_t>(gptr(d.in, d.ld_in, tf.i0 + row % T, tf.j0, false));
+        };
+        if (STEP) {
+#pragma unroll 1
+          for (int i = 0; i < 32; ++i) {
+            const int row = 32 * wl + i;
+            const TileRef& tf = ref[row / T];
+            const int rl = row % T;
+            if (tf.mi < 0) continue;
+            const MatDesc& d = descs[tf.mi];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+              const int c = ln + 32 * j;
+              const bool ok = rl < tf.h && c < tf.w;
+              const float* src = static_cast<const float*>(d.mom) +
+                                  (ok ? static_cast<int64_t>(tf.i0 + rl) * d.ld_mom + tf.j0 + c : 0);
+              ptx::cp_async_4(sbase + SM_S0 + f32_off(row, c >> 2) + (c & 3) * 4, src, ok ? 4u : 0u);
+            }
+          }
+          ptx::cp_async_commit();
+        }
+#pragma unroll 1
+        for (int rd = 0; rd < 2; ++rd) {
+          uint32_t bytes = 0;
+          uintptr_t lo = 0;
+          if ((r >> 6) == rd) {
+            const TileRef& tf = ref[r / T];
+            if (tf.mi >= 0 && r % T < tf.h) {
+              const uintptr_t a = row_src(r, tf);
+              lo = a & ~uintptr_t(15);
+              bytes = static_cast<uint32_t>(((a + 2 * tf.w + 15) & ~uintptr_t(15)) - lo);
+            }
+          }
+          if (!*abort_flag) {
+            ptx::mbar_arrive_expect_tx(b_rows, bytes);
+            if (bytes) ptx::bulk_load(sbase + SM_S1 + (r - 64 * rd) * ROWB,
+                                      reinterpret_cast<const void*>(lo), bytes, b_rows);
+          }
+          wait_bar(b_rows, rows_phase, wait_ns, abort_flag, err);
+          rows_phase ^= 1u;
+          if (STEP && rd == 0) ptx::cp_async_wait_all();   // this thread's momentum copies
+          named_sync(1, LOADER_THREADS);                    // everyone's have landed
+#pragma unroll 1
+          for (int i = 0; i < 16; ++i) {
+            const int row = 64 * rd + 16 * wl + i;
+            const TileRef& tf = ref[row / T];
+            const int rl = row % T;
+            if (tf.mi < 0) continue;                      // absent tile: zero-filled above
+            const bool row_ok = rl < tf.h;                // padding rows of the tile: zeros
+            const MatDesc& d = descs[tf.mi];
+            const uint32_t rowb = sbase + SM_S1 + (row - 64 * rd) * ROWB +
+                                  static_cast<uint32_t>(row_src(row, tf) & 15);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+              const int c = ln + 32 * j;
+              float u = 0.f;
+              if (row_ok && c < tf.w) {
+                uint16_t gb;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(gb) : "r"(rowb + 2 * c));
+                u = __uint_as_float(static_cast<uint32_t>(gb) << 16);
+                if (STEP) {
+                  const float mn = fmaf(st.mu, f32_at(sbase + SM_S0, row, c), u);
+                  st_val(d.mom, static_cast<int64_t>(tf.i0 + rl) * d.ld_mom + tf.j0 + c, true, mn);
+                  u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
+                }
+              }
+              f32_put(sbase + SM_S0, row, c, u);
+            }
+          }
+          named_sync(1, LOADER_THREADS);                    // SM_S1 is refilled next round
         }
       }
       if (any_tma) {
@@ -616,13 +750,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float s_info = ctl.info_s[t];
       // how each tile of the stage writes its weight update, copied now: the
       // loader rewrites ctl.info_* for the next stage once staging is released
-      if (STEP && issuer) {
+      if (issuer) {
 #pragma unroll
         for (int u = 0; u < TPS; ++u) {
           const int m_u = ctl.info_mi[u];
           int mode = 0;                    // transposed tiles: by the epilogue threads
-          if (m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u])
-            mode = (descs[m_u].flags & F_W_TMA) ? 1 : 2;
+          if (m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u]) {
+            const int f = descs[m_u].flags;
+            if (STEP) mode = (f & F_W_TMA) ? 1 : 2;
+            else mode = (f & F_OUT_VEC) ? 0 : 2;   // unaligned output rows: row pass
+          }
           ctl.fin_mode[s][u] = mode;
           ctl.fin_mi[s][u] = m_u;
           ctl.fin_i0[s][u] = ctl.info_i0[u];
@@ -782,7 +919,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // step: W += -lr s O by a TMA reduce-add from sC (bf16 W, no decay), or
         // O staged in sC (fp32, 64 columns at a time) for a row pass
         const bool w_red = STEP && last && mi >= 0 && !tr && (descs[mi].flags & F_W_TMA);
-        const bool w_rows = STEP && last && mi >= 0 && !tr && !w_red;
+        const bool w_rows = last && mi >= 0 && !tr && !w_red &&
+                            (STEP || !(descs[mi].flags & F_OUT_VEC));
 #pragma unroll 1
         for (int ch = 0; ch < nch; ++ch) {
           const int c = cbase + 32 * ch;
@@ -814,11 +952,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!last) hand_over(true, true, 0);   // -> next X X^T
       }
-      if (STEP) {
+      if (K > 0) {
         // the stage's -lr s O tiles are in sC: one thread adds them to W
         ptx::fence_proxy_async_smem();
         named_sync(2 + s, SLOT_THREADS);
-        if (issuer && !*abort_flag && issue_w_reduce<T>(ctl, s, maps, sc)) reduce_pending = true;
+        if (STEP && issuer && !*abort_flag && issue_w_reduce<T>(ctl, s, maps, sc)) reduce_pending = true;
         // tiles whose W is read and written here (unaligned rows, fp32 W, weight
         // decay): O is in sC (fp32, 64 columns); the slot's warps update W row by
         // row with the lanes along the columns, so that an access touches one or
@@ -827,10 +965,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < TPS; ++u) any_rows |= ctl.fin_mode[s][u] == 2;
         if (any_rows) {
-          w_row_pass<T>(ctl, s, descs, sc, 0, ws, lane, st.wd_factor);
+          w_row_pass<T, STEP>(ctl, s, descs, sc, 0, ws, lane, st.wd_factor);
           if (T == 128) {
             named_sync(2 + s, SLOT_THREADS);        // round 0 has read sC
-            if (mi >= 0 && !tr && !(descs[mi].flags & F_W_TMA) && cbase >= 64) {
+            if (mi >= 0 && !tr && (STEP ? !(descs[mi].flags & F_W_TMA) : !(descs[mi].flags & F_OUT_VEC)) &&
+                cbase >= 64) {
 #pragma unroll 1
               for (int ch = 0; ch < nch; ++ch) {
                 const int c = cbase + 32 * ch;
@@ -841,7 +980,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
             named_sync(2 + s, SLOT_THREADS);
-            w_row_pass<T>(ctl, s, descs, sc, 64, ws, lane, st.wd_factor);
+            w_row_pass<T, STEP>(ctl, s, descs, sc, 64, ws, lane, st.wd_factor);
           }
         }
       }

@@ -201,6 +201,17 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing `bytes` transaction bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Element-wise add of a shared-memory box into global memory through a tensor
 // map (the addition happens at L2; the map's data type sets the arithmetic).
 __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int32_t x,
@@ -218,6 +229,20 @@ __device__ __forceinline__ void bulk_wait_read0() {
 }
 __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cp.async (4-byte)
+// Copies 4 bytes from global to shared memory asynchronously; with src_bytes = 0
+// nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- clusters / CTA pairs
