@@ -493,6 +493,17 @@ def run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, wo
         # the next step's uploads overwrite G: they wait for this step's kernels
         up.wait_event(stepped[-1])
 
+    def copies_only():
+        # the same copies on the same streams with no compute between them: the
+        # floor the pipelined step can reach over this host link
+        for idx in groups:
+            with torch.cuda.stream(up):
+                for i in idx:
+                    Gs[i].copy_(hG[i], non_blocking=True)
+            with torch.cuda.stream(down):
+                for i in idx:
+                    hW[i].copy_(Ws[i], non_blocking=True)
+
     e2e_step()
     torch.cuda.synchronize()
     dist_barrier(world)
@@ -501,10 +512,18 @@ def run_e2e(hm, handle, Gs, Ws, Ms, shapes, T, K, chunk, flops, stream, args, wo
         e2e_step()
     torch.cuda.synchronize()
     dt = dist_max(time.perf_counter() - t0, world, dev)
+    copies_only()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    copies_only()
+    torch.cuda.synchronize()
+    floor = time.perf_counter() - t1
     return {"value": round(world * flops * n / dt / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(dt / n * 1e3, 2), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n,
-            "pipeline": f"{len(groups)} layer groups; H2D, step and D2H on three streams"}
+            "pipeline": f"{len(groups)} layer groups; H2D, step and D2H on three streams",
+            "copies_alone_ms": round(floor * 1e3, 2),
+            "copies_alone_gbs_each_way": round(h2d / floor / 1e9, 1)}
 
 
 # ---------------------------------------------------------------- secondary workloads
@@ -574,6 +593,14 @@ def _sec_gpt2(hm, handle, dev, stream, peaks, peak_src, args):
         times = _timed_b2b(fn, reps * 8, stream)
         launches = handle.launch_count() - l0
     ms = statistics.median(times)
+    # host time to issue one step call (72 matrices; tensor maps and the
+    # descriptor image come from the handle's cache after the first call)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(20):
+        fn()
+    host_us = (time.perf_counter() - t0) / 20 * 1e6
+    torch.cuda.synchronize()
     nparams = sum(H * W for H, W in shapes)
     flops = step_flops(shapes, 128, 5)
     cpu, _ = cpu_baseline(lambda i: cpu_oracle_step(768, 768, 128, 5, seed=40 + i, rank=8), cpu_s,
@@ -585,7 +612,7 @@ def _sec_gpt2(hm, handle, dev, stream, peaks, peak_src, args):
                                  "steps back to back",
              "roofline": roofline(flops, nparams * STEP_BYTES_PER_PARAM, ms * 1e-3, peaks, peak_src),
              "gpu_launches_per_run": launches / len(times), "clocks": clk.summary(),
-             "cpu_baseline": cpu}]
+             "host_us_per_call": round(host_us, 1), "cpu_baseline": cpu}]
 
 
 def _sec_sweep(hm, handle, dev, stream, peaks, peak_src, args):
