@@ -223,6 +223,7 @@ KERNEL_SOURCES = ("tiled_newton_schulz_03_b300/csrc/api.cu",
                   "tiled_newton_schulz_03_b300/csrc/kernels.h",
                   "tiled_newton_schulz_03_b300/csrc/ns_tc.cu",
                   "tiled_newton_schulz_03_b300/csrc/ptx.cuh",
+                  "tiled_newton_schulz_03_b300/csrc/tile_util.cuh",
                   "include/himuon.h")
 
 
