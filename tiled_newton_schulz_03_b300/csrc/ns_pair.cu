@@ -74,12 +74,17 @@ struct PairCtl {
   float part_peer;       // the peer CTA's sum (written by the peer)
 };
 
+// suspend-time hint (ns) of the waits on arrivals from the peer CTA or the
+// pair's tensor core
+constexpr uint32_t WAIT_HINT_NS = 20000u;
+
 // bounded wait on a local mbarrier whose arrivals may come from the peer CTA
+// (acquire at cluster scope)
 __device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                              volatile int* abort_flag, int* err) {
   if (ptx::mbar_try_wait_cluster(bar, parity, 0u)) return;
   const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait_cluster(bar, parity, 20000u)) {
+  while (!ptx::mbar_try_wait_cluster(bar, parity, WAIT_HINT_NS)) {
     if (*abort_flag) return;
     if (ptx::globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -182,8 +187,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   // tensor memory) -> product p. CTA 0's issuer waits for CTA 1's arrival.
   auto hand_over = [&](bool tmem_written, int p) {
     if (tmem_written) ptx::tmem_wait_st();
-    // E3 also wrote the peer's shared memory; E1 and E2 only this CTA's
-    if (p == 0) ptx::fence_proxy_async_cluster();
+    // Writes into the peer's shared memory (prologue, E3) are read only by the
+    // C X product (its B operand's peer block), two products later; the fence
+    // before that product covers them (a thread's fence orders all its earlier
+    // writes), so the other hand-offs need only this CTA's shared memory.
+    if (p == 2) ptx::fence_proxy_async_cluster();
     else ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
@@ -199,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   };
 
   auto wait_acc = [&]() {
-    wait_bar(b_acc, acc_ph, wait_ns, abort_flag, err);
+    wait_cluster(b_acc, acc_ph, wait_ns, abort_flag, err);   // the commit comes from CTA 0
     acc_ph ^= 1u;
     ptx::tc_fence_after();
   };
@@ -386,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
     }
     ptx::tmem_wait_st();
-    ptx::fence_proxy_async_cluster();
+    ptx::fence_proxy_async_smem();           // the peer blocks are fenced before C X
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
     // tile norm: each CTA's sum (fixed order) goes to the peer, with an arrival
@@ -415,11 +423,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       // ---- E1: A = X X^T (R_A) -> A_bf = bf16(s^2 R_A), or C = b A + e I when c = 0
       {
         wait_acc();
-#pragma unroll 1
+        float va[32], vb[32];                      // both 32-column chunks, one wait
+        ptx::tmem_ld32x2_sync(t_a + xc0, va, t_a + xc0 + 32, vb);
+#pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           const int xc = xc0 + 32 * ch;
-          float v[32];
-          ptx::tmem_ld32_sync(t_a + xc, v);
+          float (&v)[32] = ch == 0 ? va : vb;
           if (cf.has_c) {
             if (k == 0) scale32(v, s2);
           } else {
