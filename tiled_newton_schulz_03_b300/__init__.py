@@ -188,16 +188,25 @@ def _stream_ptr(stream, device) -> ctypes.c_void_p:
 
 
 def _mat_info(t: torch.Tensor, name: str):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    """(pointer, H, W, leading dimension, dtype code) of a row-major 2-D CUDA matrix.
+
+    Reads the shape and the strides as one tuple each: a step over hundreds of
+    matrices spends its host time here."""
+    try:
+        shape, strides, dt = t.shape, t.stride(), _DTYPE.get(t.dtype)
+        cuda = t.is_cuda
+    except AttributeError:
+        raise HimuonError(1, f"{name} must be a CUDA tensor") from None
+    if not cuda:
         raise HimuonError(1, f"{name} must be a CUDA tensor")
-    if t.dim() != 2:
+    if len(shape) != 2:
         raise HimuonError(1, f"{name} must be 2-D")
-    if t.dtype not in _DTYPE:
+    if dt is None:
         raise HimuonError(1, f"{name} must be bfloat16 or float32")
-    if t.size(1) > 1 and t.stride(1) != 1:
+    H, W = shape
+    if W > 1 and strides[1] != 1:
         raise HimuonError(1, f"{name} must be row-major (stride(1) == 1)")
-    ld = t.stride(0) if t.size(0) > 1 else max(t.size(1), 1)
-    return t.data_ptr(), t.size(0), t.size(1), ld, _DTYPE[t.dtype]
+    return t.data_ptr(), H, W, (strides[0] if H > 1 else max(W, 1)), dt
 
 
 def _step_schedule(coeffs, K: int):
@@ -284,15 +293,17 @@ def tiled_ns_batched(Gs, T: int, K: int = 5, coeffs=QUINTIC, norm: str = "tile",
     outs = list(outs)
     if len(outs) != len(Gs):
         raise HimuonError(1, "outs and Gs differ in length")
-    arr = (Matrix * len(Gs))()
+    rows = []
+    dev0 = Gs[0].device
     for i, (G, O) in enumerate(zip(Gs, outs)):
-        g, H, W, ldg, gt = _mat_info(G, f"Gs[{i}]")
-        o, H2, W2, ldo, ot = _mat_info(O, f"outs[{i}]")
-        if (H2, W2) != (H, W):
+        g, H, W, ldg, gt = _mat_info(G, "Gs[%d]" % i)
+        o, H2, W2, ldo, ot = _mat_info(O, "outs[%d]" % i)
+        if H2 != H or W2 != W:
             raise HimuonError(1, f"outs[{i}] must have the shape of Gs[{i}]")
-        if G.device != Gs[0].device or O.device != Gs[0].device:
+        if G.device != dev0 or O.device != dev0:
             raise HimuonError(1, "all matrices must be on one device")
-        arr[i] = Matrix(g, o, H, W, ldg, ldo, gt, ot)
+        rows.append((g, o, H, W, ldg, ldo, gt, ot))
+    arr = (Matrix * len(rows))(*rows)
     h = handle or _default_handle(Gs[0].device)
     p = _ns_params(coeffs, norm, eps, path, K)
     with torch.cuda.device(Gs[0].device):
@@ -312,14 +323,15 @@ def step(Ws, Gs, Ms, T: int, K: int = 5, lr: float = 0.02, mu: float = 0.95,
         raise HimuonError(1, "Ws, Gs and Ms must be non-empty lists of equal length")
     if scale_mode not in _SCALE:
         raise HimuonError(1, f"unknown scale mode {scale_mode!r}")
-    arr = (Param * len(Ws))()
+    rows = []
     for i, (Wt, G, M) in enumerate(zip(Ws, Gs, Ms)):
-        w, H, W, ldw, wt = _mat_info(Wt, f"Ws[{i}]")
-        g, H2, W2, ldg, gt = _mat_info(G, f"Gs[{i}]")
-        m, H3, W3, ldm, mt = _mat_info(M, f"Ms[{i}]")
-        if not ((H, W) == (H2, W2) == (H3, W3)):
+        w, H, W, ldw, wt = _mat_info(Wt, "Ws[%d]" % i)
+        g, H2, W2, ldg, gt = _mat_info(G, "Gs[%d]" % i)
+        m, H3, W3, ldm, mt = _mat_info(M, "Ms[%d]" % i)
+        if not (H == H2 == H3 and W == W2 == W3):
             raise HimuonError(1, f"shapes of Ws[{i}], Gs[{i}], Ms[{i}] differ")
-        arr[i] = Param(w, g, m, H, W, ldw, ldg, ldm, wt, gt, mt)
+        rows.append((w, g, m, H, W, ldw, ldg, ldm, wt, gt, mt))
+    arr = (Param * len(rows))(*rows)
     h = handle or _default_handle(Ws[0].device)
     p = _ns_params(coeffs, norm, eps, path, K)
     sp = StepParams(float(lr), float(mu), float(weight_decay), 1 if nesterov else 0, _SCALE[scale_mode])
