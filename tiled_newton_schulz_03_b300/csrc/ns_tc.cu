@@ -438,13 +438,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (rows_bulk) {
         // Every row of G (bf16, rows not 16-byte aligned) comes in by one bulk
         // copy of its 16-byte aligned cover (at most 15 bytes more on either
-        // side, inside the same 16-byte chunks, so always mapped memory), 64
-        // stage rows per round into SM_S1 at a stride of 2 T + 16 bytes;
+        // side, inside the same 16-byte chunks, so always mapped memory), all
+        // 128 stage rows (T = 64) or 64 per round (T = 128) into SM_S1 at a
+        // stride of 2 T + 16 bytes;
         // fp32 momentum by cp.async into the staging tile, all rows at once.
         // The warps then read each row with the lanes along the columns,
         // apply momentum (M written back, coalesced) and store U.
         constexpr int ROWB = 2 * T + 16;
         constexpr int NJ = T / 32;
+        // rows per round: all 128 when their covers fit in SM_S1 (T = 64), else 64
+        constexpr int RROWS = (128 * ROWB <= 32768) ? 128 : 64;
+        constexpr int ROUNDS = 128 / RROWS;
         const int ln = r & 31, wl = r >> 5;
         auto row_src = [&](int row, const TileRef& tf) -> uintptr_t {
           const MatDesc& d = descs[tf.mi];
@@ -470,10 +474,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ptx::cp_async_commit();
         }
 #pragma unroll 1
-        for (int rd = 0; rd < 2; ++rd) {
+        for (int rd = 0; rd < ROUNDS; ++rd) {
           uint32_t bytes = 0;
           uintptr_t lo = 0;
-          if ((r >> 6) == rd) {
+          if (r / RROWS == rd) {
             const TileRef& tf = ref[r / T];
             if (tf.mi >= 0 && r % T < tf.h) {
               const uintptr_t a = row_src(r, tf);
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           if (!*abort_flag) {
             ptx::mbar_arrive_expect_tx(b_rows, bytes);
-            if (bytes) ptx::bulk_load(sbase + SM_S1 + (r - 64 * rd) * ROWB,
+            if (bytes) ptx::bulk_load(sbase + SM_S1 + (r - RROWS * rd) * ROWB,
                                       reinterpret_cast<const void*>(lo), bytes, b_rows);
           }
           wait_bar(b_rows, rows_phase, wait_ns, abort_flag, err);
@@ -491,14 +495,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (STEP && rd == 0) ptx::cp_async_wait_all();   // this thread's momentum copies
           named_sync(1, LOADER_THREADS);                    // everyone's have landed
 #pragma unroll 1
-          for (int i = 0; i < 16; ++i) {
-            const int row = 64 * rd + 16 * wl + i;
+          for (int i = 0; i < RROWS / 4; ++i) {
+            const int row = RROWS * rd + (RROWS / 4) * wl + i;
             const TileRef& tf = ref[row / T];
             const int rl = row % T;
             if (tf.mi < 0) continue;                      // absent tile: zero-filled above
             const bool row_ok = rl < tf.h;                // padding rows of the tile: zeros
             const MatDesc& d = descs[tf.mi];
-            const uint32_t rowb = sbase + SM_S1 + (row - 64 * rd) * ROWB +
+            const uint32_t rowb = sbase + SM_S1 + (row - RROWS * rd) * ROWB +
                                   static_cast<uint32_t>(row_src(row, tf) & 15);
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
