@@ -442,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           st_bf16_32(sc, r, xc, v, pkd);
         }
       }
-      hand_over(false, cf.has_c ? 1 : 2);
+      hand_over(!cf.has_c, cf.has_c ? 1 : 2);      // before C X: the R_X stores are done
 
       if (cf.has_c) {
         // ---- E2: R_A = A_bf A_bf^T -> C = c R_A + b A_bf + e I (B at the rounded A_bf)
@@ -468,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             st_bf16_32(sc, r, xc, v, pkd);
           }
         }
-        hand_over(false, 2);
+        hand_over(true, 2);                        // the R_X stores are done
       }
 
       // ---- E3: R_X = X' (on the first step X_1 / s): the next step's operands,
@@ -476,7 +476,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       const bool last = (k + 1 == K);
       {
         wait_acc();
-        const StepCoef cfn = step_coef(ns, last ? k : k + 1);
 #pragma unroll 1
         for (int ch = 0; ch < 2; ++ch) {
           const int xc = xc0 + 32 * ch;
@@ -500,15 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             } else {
               st_bf16_32_remote(xb2_remote, r, cl, pkd);
             }
-            const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
-                                      mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
-              upk2(x, v[2 * j], v[2 * j + 1]);
-            }
-            ptx::tmem_st32(t_x + xc, v);
-            continue;
+            continue;                                // R_X after the hand-off below
           }
           // last step. A transposed tile: out = X'^T (NS map), or W <- wd W -
           // lr s X'^T (step), the lanes writing consecutive columns of one row.
@@ -596,7 +587,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         named_sync(BAR_LINK, NTHREADS);              // sC is free for the next tile
       }
-      if (!last) hand_over(true, 0);       // -> next X X^T
+      if (!last) {
+        hand_over(false, 0);                       // -> next X X^T (reads X_bf only)
+        // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
+        // step's coefficients) for that step's C X, the first product to read
+        // R_X; the hand-off before it waits for these stores.
+        const StepCoef cfn = step_coef(ns, k + 1);
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_x + xc, v);
+          if (k == 0) scale32(v, sc_t);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
+                                    mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
+            upk2(x, v[2 * j], v[2 * j + 1]);
+          }
+          ptx::tmem_st32(t_x + xc, v);
+        }
+      }
     }
   }
 

@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             st_bf16_32(sc, r, c, v, pkd);
           }
         }
-        hand_over(true, false, has_c ? 1 : 2);   // -> A A (or C X)
+        hand_over(true, !has_c, has_c ? 1 : 2);  // -> A A (or C X: R_X stores done)
 
         if (has_c) {
           // ---- E2: R_A = A_bf A_bf  ->  C = c A_bf A_bf + b A_bf + e I. The b A
@@ -912,7 +912,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t pkd[16];
             st_bf16_32(sc, r, c, v, pkd);
           }
-          hand_over(true, false, 2);       // -> C X
+          hand_over(true, true, 2);        // -> C X (R_X stores done)
         }
 
         // ---- E3: R_X = X' (on the first step X_1 / s); the next step's
@@ -943,7 +943,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
           } else {
             uint32_t pkd[16];
-            st_bf16_32(sx, r, c, v, pkd);
+            st_bf16_32(sx, r, c, v, pkd);       // the next X X^T reads only X'_bf
+          }
+        }
+        if (!last) {
+          hand_over(true, false, 0);             // -> next X X^T
+          // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
+          // step's coefficients) for that step's C X, which is the first
+          // product to read R_X; the hand-off before it waits for these stores.
+#pragma unroll 1
+          for (int ch = 0; ch < nch; ++ch) {
+            const int c = cbase + 32 * ch;
+            float v[32];
+            ptx::tmem_ld32_sync(t_x + c, v);
+            if (k == 0) scale32(v, sc_t);
+            uint32_t pkd[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
             const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -954,7 +970,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::tmem_st32(t_x + c, v);
           }
         }
-        if (!last) hand_over(true, true, 0);   // -> next X X^T
       }
       if (K > 0) {
         // the stage's -lr s O tiles are in sC: one thread adds them to W
