@@ -866,11 +866,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool has_c = cf.has_c;
         // ---- E1: A = X X^T in R_A
         wait_acc();
-#pragma unroll 1
-        for (int ch = 0; ch < nch; ++ch) {
+        // T = 128: both 32-column chunks of the thread loaded before one wait
+        float v2[NCH][32];
+        if (NCH == 2) ptx::tmem_ld32x2_sync(t_a + cbase, v2[0], t_a + cbase + 32, v2[NCH - 1]);
+        else ptx::tmem_ld32_sync(t_a + cbase, v2[0]);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
           const int c = cbase + 32 * ch;
-          float v[32];
-          ptx::tmem_ld32_sync(t_a + c, v);
+          float (&v)[32] = v2[ch];
           uint32_t pkd[16];
           if (has_c) {
             if (k == 0) scale32(v, s2);              // A = s^2 U_bf U_bf^T
