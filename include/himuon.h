@@ -87,7 +87,10 @@ typedef enum {
  * p_k(s) = a_k s + b_k s^3 + c_k s^5 on the singular values. A step with
  * c_k = 0 is a cubic step (two products instead of three), e.g. the classical
  * polar iteration (1.5, -0.5, 0). The abstract fixes neither the coefficients
- * nor that they are constant; both readings are parameters here.
+ * nor that they are constant; both readings are parameters here. Every
+ * coefficient must be finite, and a step with c_k != 0 must have |b_k / c_k|
+ * and |e_k / c_k| <= 1e30, where e_k = a_k - min(a_k, 1.5) (HIMUON_ERR_INVALID_ARG
+ * otherwise; the on-chip kernels start the A A accumulator at those ratios).
  */
 typedef struct {
   float a, b, c;   /* NS coefficients of every step when step_coeffs is NULL */

@@ -146,6 +146,22 @@ def test_schedule_errors():
     with pytest.raises(hm.HimuonError) as e:              # checked on the host, nothing launched
         hm.tiled_ns(G, 64, 5, coeffs=bad)
     assert e.value.status_name == "INVALID_ARG" and "step 2" in str(e.value)
+    tiny_c = list(SCHED)
+    tiny_c[1] = (3.0, -1.0, 1e-35)                        # b / c beyond 1e30
+    with pytest.raises(hm.HimuonError) as e:
+        hm.tiled_ns(G, 64, 5, coeffs=tiny_c)
+    assert e.value.status_name == "INVALID_ARG" and "step 1" in str(e.value)
+
+
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_small_c_step_matches_oracle(T):
+    # b / c = -12500 and e / c = 1250: the on-chip kernels' A A accumulator
+    # starts at those multiples of A_bf and I, and c scales the sum back
+    sched = [hm.QUINTIC] * 2 + [(1.625, -1.0, 8e-5)] + [hm.QUINTIC] * 2
+    G = synth.lowrank_noise(320, 448, seed=T + 11)
+    out = hm.tiled_ns(G.cuda(), T, 5, coeffs=sched, out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), T, 5, sched)
+    assert rel_fro(f64(out), want) <= TOL_BF16
 
 
 # ---------------------------------------------------------------- bit-exact structure

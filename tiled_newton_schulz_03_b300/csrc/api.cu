@@ -94,6 +94,11 @@ himuon_status make_ns_args(const himuon_ns_params& p, int32_t K, int32_t T, NSAr
         !std::isfinite(ns->coef[k][2]))
       return fail(HIMUON_ERR_INVALID_ARG,
                   "ns params: coefficients of step " + std::to_string(k) + " must be finite");
+    // the on-chip kernels start the A A accumulator at (b / c) A_bf + (e / c) I
+    const StepCoef sc = step_coef(*ns, k);
+    if (sc.has_c && !(std::fabs(sc.bc) <= 1e30f && std::fabs(sc.ec) <= 1e30f))
+      return fail(HIMUON_ERR_INVALID_ARG,
+                  "ns params: step " + std::to_string(k) + ": c must be 0 or |b / c|, |e / c| <= 1e30");
   }
   return HIMUON_OK;
 }

@@ -69,6 +69,7 @@ struct NSArgs {
 // tensor-core kernels move from a X into the bf16 operand C = B + e I.
 struct StepCoef {
   float a, b, c, e;
+  float bc, ec;      // b / c and e / c (c != 0): R_A starts at (b / c) A_bf + (e / c) I
   bool has_c;        // c != 0: the step needs the product A A
 };
 
@@ -79,6 +80,8 @@ __host__ __device__ __forceinline__ StepCoef step_coef(const NSArgs& ns, int k) 
   s.c = ns.coef[k][2];
   s.e = s.a > 1.5f ? s.a - 1.5f : 0.f;
   s.has_c = s.c != 0.f;
+  s.bc = s.has_c ? s.b / s.c : 0.f;
+  s.ec = s.has_c ? s.e / s.c : 0.f;
   return s;
 }
 

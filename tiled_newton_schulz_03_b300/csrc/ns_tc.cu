@@ -598,7 +598,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           } else {
             bd = ptx::sdesc_sw128(a_base + u * T * 128 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
           }
-          const uint32_t accum = (p == 2 || kk > 0) ? 1u : 0u;   // C X onto a X - e X_bf
+          // A A onto (b / c) A_bf + (e / c) I, C X onto a X - e X_bf
+          const uint32_t accum = (p != 0 || kk > 0) ? 1u : 0u;
           ptx::umma_bf16(dcol + u * T, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, accum);
         }
       }
@@ -878,6 +879,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (has_c) {
             if (k == 0) scale32(v, s2);              // A = s^2 U_bf U_bf^T
             st_bf16_32(sc, r, c, v, pkd);            // A_bf
+            // R_A <- (b / c) A_bf + (e / c) I, onto which A A accumulates, so
+            // that c R_A = c A_bf A_bf + b A_bf + e I: B is evaluated at the
+            // same rounded A_bf as the product, whose rounding then enters
+            // through dB/dA = b + 2 c A, small where the two terms nearly
+            // cancel, instead of through 2 c A alone
+            const uint64_t bc2 = pk2(cf.bc, cf.bc);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              uint64_t x = mul2(bc2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j])));
+              upk2(x, v[2 * j], v[2 * j + 1]);
+            }
+            if ((rl >> 5) == (c >> 5)) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? cf.ec : 0.f;
+            }
+            ptx::tmem_st32(t_a + c, v);
           } else {
             scale32(v, k == 0 ? cf.b * s2 : cf.b);   // C = b A + e I
             if ((rl >> 5) == (c >> 5)) {
@@ -887,33 +904,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             st_bf16_32(sc, r, c, v, pkd);
           }
         }
-        hand_over(true, !has_c, has_c ? 1 : 2);  // -> A A (or C X: R_X stores done)
+        hand_over(true, true, has_c ? 1 : 2);    // -> A A onto R_A (or C X: R_X stores done)
 
         if (has_c) {
-          // ---- E2: R_A = A_bf A_bf  ->  C = c A_bf A_bf + b A_bf + e I. The b A
-          // term takes the same rounded A_bf as the product (read back from sC),
-          // so B is evaluated exactly at A_bf and its rounding enters through
-          // dB/dA = b + 2 c A, small where the two terms nearly cancel, instead
-          // of through 2 c A alone.
+          // ---- E2: R_A = A_bf A_bf + (b / c) A_bf + (e / c) I  ->  C = c R_A
           wait_acc();
-#pragma unroll 1
-          for (int ch = 0; ch < nch; ++ch) {
-            const int c = cbase + 32 * ch;
-            float v[32], av[32];
-            ld_bf16_32(sc, r, c, av);                // in flight during the TMEM load
-            ptx::tmem_ld32_sync(t_a + c, v);
-            const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
+          float v2[NCH][32];
+          if (NCH == 2) ptx::tmem_ld32x2_sync(t_a + cbase, v2[0], t_a + cbase + 32, v2[NCH - 1]);
+          else ptx::tmem_ld32_sync(t_a + cbase, v2[0]);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              uint64_t x = fma2(c2, pk2(v[j], v[j + 1]), mul2(b2, pk2(av[j], av[j + 1])));
-              upk2(x, v[j], v[j + 1]);
-            }
-            if ((rl >> 5) == (c >> 5)) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
-            }
+          for (int ch = 0; ch < NCH; ++ch) {
+            scale32(v2[ch], cf.c);
             uint32_t pkd[16];
-            st_bf16_32(sc, r, c, v, pkd);
+            st_bf16_32(sc, r, cbase + 32 * ch, v2[ch], pkd);
           }
           hand_over(true, true, 2);        // -> C X (R_X stores done)
         }
@@ -928,13 +931,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool w_red = STEP && last && mi >= 0 && !tr && (descs[mi].flags & F_W_TMA);
         const bool w_rows = last && mi >= 0 && !tr && !w_red &&
                             (STEP || !(descs[mi].flags & F_OUT_VEC));
+        if (!last) {
+          // the next X X^T reads only X'_bf; T = 128: both chunks loaded before one wait
+          {
+            float v2[NCH][32];
+            if (NCH == 2) ptx::tmem_ld32x2_sync(t_x + cbase, v2[0], t_x + cbase + 32, v2[NCH - 1]);
+            else ptx::tmem_ld32_sync(t_x + cbase, v2[0]);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              if (k == 0) scale32(v2[ch], sc_t);
+              uint32_t pkd[16];
+              st_bf16_32(sx, r, cbase + 32 * ch, v2[ch], pkd);
+            }
+          }
+          hand_over(true, false, 0);             // -> next X X^T
+          // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
+          // step's coefficients) for that step's C X, which is the first
+          // product to read R_X; the hand-off before it waits for these stores.
+          float v2[NCH][32];
+          if (NCH == 2) ptx::tmem_ld32x2_sync(t_x + cbase, v2[0], t_x + cbase + 32, v2[NCH - 1]);
+          else ptx::tmem_ld32_sync(t_x + cbase, v2[0]);
+          const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            float (&v)[32] = v2[ch];
+            if (k == 0) scale32(v, sc_t);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t pb = ptx::pack_bf16x2(v[j], v[j + 1]);
+              uint64_t x = fma2(a2, pk2(v[j], v[j + 1]), mul2(ne2, pk2(ptx::bf16lo(pb), ptx::bf16hi(pb))));
+              upk2(x, v[j], v[j + 1]);
+            }
+            ptx::tmem_st32(t_x + cbase + 32 * ch, v);
+          }
+        } else {
 #pragma unroll 1
-        for (int ch = 0; ch < nch; ++ch) {
-          const int c = cbase + 32 * ch;
-          float v[32];
-          ptx::tmem_ld32_sync(t_x + c, v);
-          if (k == 0) scale32(v, sc_t);
-          if (last) {
+          for (int ch = 0; ch < nch; ++ch) {
+            const int c = cbase + 32 * ch;
+            float v[32];
+            ptx::tmem_ld32_sync(t_x + c, v);
+            if (k == 0) scale32(v, sc_t);
             if (w_red) {
               scale32(v, -descs[mi].upd_scale);     // -lr s O, added to W by TMA below
               uint32_t pkd[16];
@@ -944,33 +980,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else if (mi >= 0) {
               emit(descs[mi], i0, j0, th, tw, tr, c, v);
             }
-          } else {
-            uint32_t pkd[16];
-            st_bf16_32(sx, r, c, v, pkd);       // the next X X^T reads only X'_bf
-          }
-        }
-        if (!last) {
-          hand_over(true, false, 0);             // -> next X X^T
-          // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
-          // step's coefficients) for that step's C X, which is the first
-          // product to read R_X; the hand-off before it waits for these stores.
-#pragma unroll 1
-          for (int ch = 0; ch < nch; ++ch) {
-            const int c = cbase + 32 * ch;
-            float v[32];
-            ptx::tmem_ld32_sync(t_x + c, v);
-            if (k == 0) scale32(v, sc_t);
-            uint32_t pkd[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
-            const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
-                                mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
-              upk2(x, v[2 * j], v[2 * j + 1]);
-            }
-            ptx::tmem_st32(t_x + c, v);
           }
         }
       }
