@@ -177,7 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         bd = (p == 1) ? ad
                       : ptx::sdesc_sw128(sbase + sm_b(2 + (kk >> 3)) + (kk & 7) * 16 * 128, 16384, 1024);
       }
-      ptx::umma_bf16_pair(dcol, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, (p == 2 || kk > 0) ? 1u : 0u);
+      // A A onto (b / c) A_bf + (e / c) I, C X onto a X - e X_bf
+      ptx::umma_bf16_pair(dcol, ad, bd, p == 2 ? IDESC_KM : IDESC_KK, (p != 0 || kk > 0) ? 1u : 0u);
     }
     ptx::umma_commit_pair_mc(b_acc, 0x3);
     issued = true;
@@ -420,7 +421,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     for (int k = 0; k < K; ++k) {
       const StepCoef cf = step_coef(ns, k);
       const float e = cf.e;
-      // ---- E1: A = X X^T (R_A) -> A_bf = bf16(s^2 R_A), or C = b A + e I when c = 0
+      // ---- E1: A = X X^T (R_A) -> A_bf = bf16(s^2 R_A) and R_A <- (b / c) A_bf +
+      // (e / c) I, onto which A A accumulates (c R_A = c A_bf A_bf + b A_bf + e I:
+      // B is evaluated at the same rounded A_bf as the product); or C = b A + e I
+      // when c = 0
       {
         wait_acc();
         float va[32], vb[32];                      // both 32-column chunks, one wait
@@ -429,44 +433,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         for (int ch = 0; ch < 2; ++ch) {
           const int xc = xc0 + 32 * ch;
           float (&v)[32] = ch == 0 ? va : vb;
+          const bool diag = (xr >> 5) == (xc >> 5);
+          uint32_t pkd[16];
           if (cf.has_c) {
             if (k == 0) scale32(v, s2);
+            st_bf16_32(sc, r, xc, v, pkd);
+            const uint64_t bc2 = pk2(cf.bc, cf.bc);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              upk2(mul2(bc2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))), v[2 * j], v[2 * j + 1]);
+            if (diag) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? cf.ec : 0.f;
+            }
+            ptx::tmem_st32(t_a + xc, v);
           } else {
             scale32(v, k == 0 ? cf.b * s2 : cf.b);
-            if ((xr >> 5) == (xc >> 5)) {
+            if (diag) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
             }
-          }
-          uint32_t pkd[16];
-          st_bf16_32(sc, r, xc, v, pkd);
-        }
-      }
-      hand_over(!cf.has_c, cf.has_c ? 1 : 2);      // before C X: the R_X stores are done
-
-      if (cf.has_c) {
-        // ---- E2: R_A = A_bf A_bf^T -> C = c R_A + b A_bf + e I (B at the rounded A_bf)
-        {
-          wait_acc();
-#pragma unroll 1
-          for (int ch = 0; ch < 2; ++ch) {
-            const int xc = xc0 + 32 * ch;
-            float v[32], av[32];
-            ld_bf16_32(sc, r, xc, av);               // in flight during the TMEM load
-            ptx::tmem_ld32_sync(t_a + xc, v);
-            const uint64_t c2 = pk2(cf.c, cf.c), b2 = pk2(cf.b, cf.b);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const uint64_t x = fma2(c2, pk2(v[j], v[j + 1]), mul2(b2, pk2(av[j], av[j + 1])));
-              upk2(x, v[j], v[j + 1]);
-            }
-            if ((xr >> 5) == (xc >> 5)) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] += (j == lane) ? e : 0.f;
-            }
-            uint32_t pkd[16];
             st_bf16_32(sc, r, xc, v, pkd);
           }
+        }
+      }
+      hand_over(true, cf.has_c ? 1 : 2);           // R_A preload (or, before C X, R_X) stored
+
+      if (cf.has_c) {
+        // ---- E2: R_A = A_bf A_bf^T + (b / c) A_bf + (e / c) I -> C = c R_A
+        {
+          wait_acc();
+          float va[32], vb[32];
+          ptx::tmem_ld32x2_sync(t_a + xc0, va, t_a + xc0 + 32, vb);
+          scale32(va, cf.c);
+          scale32(vb, cf.c);
+          uint32_t pkd[16];
+          st_bf16_32(sc, r, xc0, va, pkd);
+          st_bf16_32(sc, r, xc0 + 32, vb, pkd);
         }
         hand_over(true, 2);                        // the R_X stores are done
       }
@@ -476,13 +479,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       const bool last = (k + 1 == K);
       {
         wait_acc();
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-          const int xc = xc0 + 32 * ch;
-          float v[32];
-          ptx::tmem_ld32_sync(t_x + xc, v);
-          if (k == 0) scale32(v, sc_t);
-          if (!last) {
+        if (!last) {
+          float va[32], vb[32];                    // both 32-column chunks, one wait
+          ptx::tmem_ld32x2_sync(t_x + xc0, va, t_x + xc0 + 32, vb);
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int xc = xc0 + 32 * ch;
+            float (&v)[32] = ch == 0 ? va : vb;
+            if (k == 0) scale32(v, sc_t);
             uint32_t pkd[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
@@ -499,8 +503,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             } else {
               st_bf16_32_remote(xb2_remote, r, cl, pkd);
             }
-            continue;                                // R_X after the hand-off below
-          }
+          }                                          // R_X after the hand-off below
+        }
+#pragma unroll 1
+        for (int ch = 0; ch < 2 && last; ++ch) {
+          const int xc = xc0 + 32 * ch;
+          float v[32];
+          ptx::tmem_ld32_sync(t_x + xc, v);
+          if (k == 0) scale32(v, sc_t);
           // last step. A transposed tile: out = X'^T (NS map), or W <- wd W -
           // lr s X'^T (step), the lanes writing consecutive columns of one row.
           if (!tr && vec_out) {                      // 16-byte stores of the own row segment
@@ -593,23 +603,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // step's coefficients) for that step's C X, the first product to read
         // R_X; the hand-off before it waits for these stores.
         const StepCoef cfn = step_coef(ns, k + 1);
-#pragma unroll 1
+        float va[32], vb[32];                      // both 32-column chunks, one wait
+        ptx::tmem_ld32x2_sync(t_x + xc0, va, t_x + xc0 + 32, vb);
+        const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
+#pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
-          const int xc = xc0 + 32 * ch;
-          float v[32];
-          ptx::tmem_ld32_sync(t_x + xc, v);
+          float (&v)[32] = ch == 0 ? va : vb;
           if (k == 0) scale32(v, sc_t);
-          uint32_t pkd[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(v[2 * j], v[2 * j + 1]);
-          const uint64_t a2 = pk2(cfn.a, cfn.a), ne2 = pk2(-cfn.e, -cfn.e);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint64_t x = fma2(a2, pk2(v[2 * j], v[2 * j + 1]),
-                                    mul2(ne2, pk2(ptx::bf16lo(pkd[j]), ptx::bf16hi(pkd[j]))));
-            upk2(x, v[2 * j], v[2 * j + 1]);
+          for (int j = 0; j < 32; j += 2) {
+            const uint32_t pb = ptx::pack_bf16x2(v[j], v[j + 1]);
+            const uint64_t x = fma2(a2, pk2(v[j], v[j + 1]), mul2(ne2, pk2(ptx::bf16lo(pb), ptx::bf16hi(pb))));
+            upk2(x, v[j], v[j + 1]);
           }
-          ptx::tmem_st32(t_x + xc, v);
+          ptx::tmem_st32(t_x + xc0 + 32 * ch, v);
         }
       }
     }
