@@ -67,33 +67,12 @@ constexpr uint32_t SMEM_DYN = SM_END + 1024;
 
 struct PairCtl {
   uint64_t acc_full;     // the pair's last product is complete (multicast commit)
-  uint64_t peer_ready;   // the peer CTA's tile-norm partial sum has arrived
   uint64_t drain;        // abort path: every issued product has completed
   uint32_t tmem_base;
   int abort_flag;
   float part[16];        // per warp: sum of squares of its elements
   float part_peer;       // the peer CTA's sum (written by the peer)
 };
-
-// suspend-time hint (ns) of the waits on arrivals from the peer CTA or the
-// pair's tensor core
-constexpr uint32_t WAIT_HINT_NS = 20000u;
-
-// bounded wait on a local mbarrier whose arrivals may come from the peer CTA
-// (acquire at cluster scope)
-__device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                             volatile int* abort_flag, int* err) {
-  if (ptx::mbar_try_wait_cluster(bar, parity, 0u)) return;
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait_cluster(bar, parity, WAIT_HINT_NS)) {
-    if (*abort_flag) return;
-    if (ptx::globaltimer() - t0 > limit_ns) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, DEV_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
 
 // 32 bf16 values -> 4 x 16-byte chunks of row r, columns [c, c + 32), of a
 // swizzled bf16 buffer in the PEER's shared memory (cluster address of its base)
@@ -120,12 +99,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const uint32_t peer = c ^ 1u;
   volatile int* abort_flag = &ctl.abort_flag;
   const uint32_t b_acc = ptx::smem_u32(&ctl.acc_full);
-  const uint32_t b_peer = ptx::smem_u32(&ctl.peer_ready);
   const uint32_t b_drain = ptx::smem_u32(&ctl.drain);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(b_acc, 1);
-    ptx::mbar_init(b_peer, 1);
     ptx::mbar_init(b_drain, 1);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
@@ -157,7 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const uint32_t xb2_local = sbase + sm_b(2 + static_cast<int>(c));
   const uint32_t xb2_remote = ptx::mapa_shared(sbase + sm_b(2 + static_cast<int>(c)), peer);
 
-  uint32_t acc_ph = 0, pr_ph = 0;
+  uint32_t acc_ph = 0;
   bool issued = false;
 
   // product p of the tile (0: X X^T -> R_A; 1: A A^T -> R_A; 2: C X onto R_X)
@@ -202,8 +179,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     issue(p);                                  // CTA 0's issuer only
   };
 
+  // The commit that completes acc_full comes from CTA 0's issuer, multicast by
+  // the tensor core; what it orders is tensor memory, which the
+  // tcgen05.fence::after_thread_sync below covers, so the wait needs CTA scope only.
   auto wait_acc = [&]() {
-    wait_cluster(b_acc, acc_ph, wait_ns, abort_flag, err);   // the commit comes from CTA 0
+    wait_bar(b_acc, acc_ph, wait_ns, abort_flag, err);
     acc_ph ^= 1u;
     ptx::tc_fence_after();
   };
@@ -394,17 +374,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     else ptx::fence_proxy_async_cluster();   // this thread also wrote the peer's block
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
-    // tile norm: each CTA's sum (fixed order) goes to the peer, with an arrival
+    // tile norm: each CTA's sum (fixed order) goes to the peer; the cluster
+    // barrier after it is also the hand-off of the prologue's operands
     float part_self = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) part_self += ctl.part[i];
-    if (threadIdx.x == 0 && !*abort_flag) {
+    if (threadIdx.x == 0)
       ptx::st_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&ctl.part_peer), peer), part_self);
-      ptx::mbar_arrive_cluster(ptx::mapa_shared(b_peer, peer));
-    }
-    wait_cluster(b_peer, pr_ph, wait_ns, abort_flag, err);
-    pr_ph ^= 1u;
-    named_sync(BAR_LINK, NTHREADS);        // no thread of CTA 0 lags a phase behind the issuer
+    ptx::cluster_sync();
     const float tot = (c == 0) ? part_self + ctl.part_peer : ctl.part_peer + part_self;
     float sc_t = 1.f;
     if (ns.norm == NORM_TILE) sc_t = 1.f / (sqrtf(tot) + ns.eps);
