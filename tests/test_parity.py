@@ -309,9 +309,10 @@ def test_step_weight_reduce_add_is_one_rounding_of_w_plus_update(T, H, W):
     update by a TMA reduce-add of D = bf16(-lr s O) onto W. From W0 = 0 the step
     stores D itself; from any W0 (same G and M) it must store bf16_rne(W0 + D),
     element for element. Shapes with aligned rows and tall or full tiles only
-    (unaligned rows and wide edge tiles take the read-modify-write, one rounding
-    of W0 + fp32 update); right-edge tiles narrower than a 64-column box (8 and
-    8 columns at 520 and 200) check the box clipping."""
+    (unaligned rows are the next test's; wide edge tiles take the
+    read-modify-write, one rounding of W0 + fp32 update); right-edge tiles
+    narrower than a 64-column box (8 and 8 columns at 520 and 200) check the box
+    clipping."""
     G = synth.lowrank_noise(H, W, seed=T + H).cuda()
     M0 = synth.gaussian(H, W, 3, std=1e-3).cuda()
     W0 = synth.gaussian(H, W, 4, std=0.02, dtype=torch.bfloat16).cuda()
@@ -326,11 +327,35 @@ def test_step_weight_reduce_add_is_one_rounding_of_w_plus_update(T, H, W):
     check_update(f64(Wz), np.zeros((H, W)), Wn, TOL_BF16)
 
 
+@pytest.mark.parametrize("T,H,W", [(128, 256, 521), (128, 128, 515), (64, 192, 203), (64, 128, 131)])
+def test_step_unaligned_bf16_rows_one_rounding(T, H, W):
+    """bf16 weights whose rows are not 16-byte aligned (odd widths), no weight
+    decay: each row's 16-byte aligned interior gets D = bf16(-lr s O) by one bulk
+    reduce-add and the elements outside it by single atomic adds. From W0 = 0
+    the step stores D; from any W0 (same G and M) it must store bf16_rne(W0 + D),
+    element for element. H is a multiple of T, so no tile runs transposed; the
+    right-edge tiles (9, 3, 11 and 3 columns) are narrower than one 16-byte
+    chunk plus a phase, so some rows have no interior at all."""
+    G = synth.lowrank_noise(H, W, seed=T + W).cuda()
+    M0 = synth.gaussian(H, W, 5, std=1e-3).cuda()
+    W0 = synth.gaussian(H, W, 6, std=0.02, dtype=torch.bfloat16).cuda()
+    Wz, Mz = torch.zeros_like(W0), M0.clone()
+    hm.step([Wz], [G], [Mz], T, 5, lr=0.02, mu=0.95, path="tensor")
+    Wa, Ma = W0.clone(), M0.clone()
+    hm.step([Wa], [G], [Ma], T, 5, lr=0.02, mu=0.95, path="tensor")
+    assert torch.equal(Ma, Mz)
+    want = (W0.float() + Wz.float()).to(torch.bfloat16)
+    assert torch.equal(Wa, want)
+    Wn, _, _ = oracle.himuon_step(np.zeros((H, W)), f64(G), f64(M0), T, 5, lr=0.02, mu=0.95)
+    check_update(f64(Wz), np.zeros((H, W)), Wn, TOL_BF16)
+
+
 @pytest.mark.parametrize("T", [64, 128])
 def test_step_mixed_weight_update_paths(T):
-    """Weights updated three ways in one call: aligned bf16 rows by TMA
-    reduce-add, unaligned rows (odd widths) and fp32 weights by the row pass,
-    wide edge tiles by the epilogue threads. Odd tile counts at T = 64 put tiles
+    """Weights updated four ways in one call: aligned bf16 rows by TMA
+    reduce-add, unaligned bf16 rows (odd widths) by bulk reduce-adds of their
+    aligned interiors, fp32 weights by the row pass, wide edge tiles by the
+    epilogue threads. Odd tile counts at T = 64 put tiles
     of different paths into one stacked stage."""
     shapes = [(192, 320), (130, 203), (64, 64), (200, 530), (70, 300)]
     dtypes = [torch.bfloat16, torch.bfloat16, torch.float32, torch.bfloat16, torch.float32]

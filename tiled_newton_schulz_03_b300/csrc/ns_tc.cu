@@ -89,8 +89,8 @@ struct Ctl {
   int ticket_s[2];        // the stage each slot took
   // per slot and stacked tile, copied from info_* when the slot takes a stage:
   // how the step's weight update is written (fin_mode: 0 by the epilogue
-  // threads, 1 TMA reduce-add of -lr s O, 2 row pass from sC), matrix, origin
-  // and extent
+  // threads, 1 TMA reduce-add of -lr s O, 2 row pass from sC, 3 bulk
+  // reduce-add of each row's 16-byte aligned interior), matrix, origin and extent
   int fin_mode[2][2], fin_mi[2][2], fin_i0[2][2], fin_j0[2][2], fin_h[2][2], fin_w[2][2];
 };
 
@@ -577,6 +577,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool issuer = (ws == pw && lane == 0);
     bool issued = false;
     bool reduce_pending = false;   // issuer: a TMA reduce-add still reads sC
+    bool rows_pending = false;     // a bulk reduce-add of a W row still reads sX
+    // bf16 weights without decay whose rows TMA cannot describe: the last
+    // epilogue writes bf16(-lr s O) into one shared-memory line per stage row
+    // (sX and sC, free after the last product) with the row's 16-byte phase,
+    // one thread per row adds the row's 16-byte aligned interior to W with a
+    // bulk reduce-add (at L2, no read of W into the SM), and the few elements
+    // outside it are added one by one with atomic adds
+    auto bulk_rows = [&](int f) {
+      return STEP && !(f & F_W_TMA) && !(f & F_OUT_FP32) && st.wd_factor == 1.f;
+    };
+    constexpr uint32_t LROW = 2 * T + 16;   // bytes per line: the row and its phase
 
     // Product p of this slot (0: X X^T -> R_A; 1: A A onto R_A; 2: C X onto R_X),
     // one 128 x T x T MMA per stacked tile, completion signalled on acc_full[s].
@@ -740,6 +751,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // g is signalled on st_full[g % 2]; the two slots hold consecutive tickets,
     // so they never wait on the same barrier at different phases.
     for (;;) {
+      if (rows_pending) {                  // the next prologue rewrites sX
+        ptx::bulk_wait_read0();
+        rows_pending = false;
+      }
       if (issuer) ctl.ticket_s[s] = atomicAdd(&ctl.ticket, 1);
       named_sync(2 + s, SLOT_THREADS);
       const int64_t g = ctl.ticket_s[s];
@@ -762,7 +777,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           int mode = 0;                    // transposed tiles: by the epilogue threads
           if (m_u >= 0 && ctl.info_h[u] >= ctl.info_w[u]) {
             const int f = descs[m_u].flags;
-            if (STEP) mode = (f & F_W_TMA) ? 1 : 2;
+            if (STEP) mode = (f & F_W_TMA) ? 1 : bulk_rows(f) ? 3 : 2;
             else mode = (f & F_OUT_VEC) ? 0 : 2;   // unaligned output rows: row pass
           }
           ctl.fin_mode[s][u] = mode;
@@ -787,11 +802,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (STEP && mi >= 0 && !tr && !(descs[mi].flags & F_W_TMA) && rl < th && cbase < tw) {
         // the weights this thread updates at the end of the tile: pull them into
         // L2 now, so that the final update does not wait on DRAM
+        // (every 128-byte line the row segment touches, whatever its alignment)
         const MatDesc& d = descs[mi];
         const bool out32 = d.flags & F_OUT_FP32;
         const char* wp = gptr(d.out, d.ld_out, i0 + rl, j0 + cbase, out32);
+        const int seg = HALF * (out32 ? 4 : 2);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(wp));
-        if (out32 && HALF * 4 > 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(wp + 128));
+        if (seg > 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(wp + 128));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(wp + seg - 1));
       }
       float ssq = 0.f;
 #pragma unroll 1
@@ -929,7 +947,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // step: W += -lr s O by a TMA reduce-add from sC (bf16 W, no decay), or
         // O staged in sC (fp32, 64 columns at a time) for a row pass
         const bool w_red = STEP && last && mi >= 0 && !tr && (descs[mi].flags & F_W_TMA);
-        const bool w_rows = last && mi >= 0 && !tr && !w_red &&
+        const bool w_bulk = last && mi >= 0 && !tr && !w_red && bulk_rows(descs[mi].flags);
+        const bool w_rows = last && mi >= 0 && !tr && !w_red && !w_bulk &&
                             (STEP || !(descs[mi].flags & F_OUT_VEC));
         if (!last) {
           // the next X X^T reads only X'_bf; T = 128: both chunks loaded before one wait
@@ -977,6 +996,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               st_bf16_32(sc, r, c, v, pkd);
             } else if (w_rows) {
               if (c < 64) st_f32_32(sc, r, c, v);   // columns [64, 128) in a second round
+            } else if (w_bulk) {
+              const MatDesc& d = descs[mi];
+              const uintptr_t g0 = reinterpret_cast<uintptr_t>(gptr(d.out, d.ld_out, i0 + rl, j0, false));
+              const uintptr_t ga = (g0 + 15) & ~uintptr_t(15);
+              const uintptr_t gb = (g0 + 2 * static_cast<uintptr_t>(tw)) & ~uintptr_t(15);
+              const uint32_t line = sbase + sm_x(s) + static_cast<uint32_t>(r) * LROW +
+                                    static_cast<uint32_t>(g0 & 15);
+              const float nls = -d.upd_scale;
+              if (rl < th) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int col = c + j;
+                  if (col < tw) {
+                    const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(nls * v[j]));
+                    const uintptr_t ge = g0 + 2 * static_cast<uintptr_t>(col);
+                    if (ge >= ga && ge < gb)
+                      asm volatile("st.shared.u16 [%0], %1;" ::"r"(line + 2u * col), "h"(bits) : "memory");
+                    else
+                      ptx::red_add_bf16(reinterpret_cast<void*>(ge), bits);
+                  }
+                }
+              }
             } else if (mi >= 0) {
               emit(descs[mi], i0, j0, th, tw, tr, c, v);
             }
@@ -988,6 +1029,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::fence_proxy_async_smem();
         named_sync(2 + s, SLOT_THREADS);
         if (STEP && issuer && !*abort_flag && issue_w_reduce<T>(ctl, s, maps, sc)) reduce_pending = true;
+        if (STEP && mi >= 0 && !tr && bulk_rows(descs[mi].flags) && cbase == 0 && rl < th && !*abort_flag) {
+          // this row's interior, written into its line by the row's threads above
+          const MatDesc& d = descs[mi];
+          const uintptr_t g0 = reinterpret_cast<uintptr_t>(gptr(d.out, d.ld_out, i0 + rl, j0, false));
+          const uintptr_t ga = (g0 + 15) & ~uintptr_t(15);
+          const uintptr_t gb = (g0 + 2 * static_cast<uintptr_t>(tw)) & ~uintptr_t(15);
+          if (gb > ga) {
+            ptx::bulk_reduce_add_bf16(reinterpret_cast<void*>(ga),
+                                      sbase + sm_x(s) + static_cast<uint32_t>(r) * LROW +
+                                          static_cast<uint32_t>(ga - (g0 & ~uintptr_t(15))),
+                                      static_cast<uint32_t>(gb - ga));
+            ptx::bulk_commit();
+            rows_pending = true;
+          }
+        }
         // tiles whose W is read and written here (unaligned rows, fp32 W, weight
         // decay): O is in sC (fp32, 64 columns); the slot's warps update W row by
         // row with the lanes along the columns, so that an access touches one or
@@ -1016,7 +1072,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    if (reduce_pending) ptx::bulk_wait0();     // the reduces have completed before exit
+    if (reduce_pending || rows_pending) ptx::bulk_wait0();   // the reduces have completed before exit
 
     if (issued && *abort_flag) {
       // let every MMA this slot issued finish before tensor memory is released

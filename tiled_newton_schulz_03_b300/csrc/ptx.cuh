@@ -221,6 +221,19 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src
       ::"l"(tmap), "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+// Element-wise bf16 add of `bytes` bytes of shared memory into global memory
+// (no tensor map; the addition happens at L2). dst and src 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_reduce_add_bf16(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.noftz.bf16 [%0], [%1], %2;"
+      ::"l"(dst), "r"(src), "r"(bytes)
+      : "memory");
+}
+// Atomic bf16 add of one element into global memory (rounded once to bf16).
+__device__ __forceinline__ void red_add_bf16(void* dst, uint16_t bits) {
+  asm volatile("red.relaxed.gpu.global.add.noftz.bf16 [%0], %1;" ::"l"(dst), "h"(bits) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
