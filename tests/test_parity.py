@@ -327,15 +327,17 @@ def test_step_weight_reduce_add_is_one_rounding_of_w_plus_update(T, H, W):
     check_update(f64(Wz), np.zeros((H, W)), Wn, TOL_BF16)
 
 
-@pytest.mark.parametrize("T,H,W", [(128, 256, 521), (128, 128, 515), (64, 192, 203), (64, 128, 131)])
+@pytest.mark.parametrize("T,H,W", [(128, 256, 521), (128, 128, 515), (64, 192, 203), (64, 128, 131),
+                                   (256, 256, 521), (256, 512, 520), (200, 400, 411)])
 def test_step_unaligned_bf16_rows_one_rounding(T, H, W):
-    """bf16 weights whose rows are not 16-byte aligned (odd widths), no weight
-    decay: each row's 16-byte aligned interior gets D = bf16(-lr s O) by one bulk
-    reduce-add and the elements outside it by single atomic adds. From W0 = 0
-    the step stores D; from any W0 (same G and M) it must store bf16_rne(W0 + D),
-    element for element. H is a multiple of T, so no tile runs transposed; the
-    right-edge tiles (9, 3, 11 and 3 columns) are narrower than one 16-byte
-    chunk plus a phase, so some rows have no interior at all."""
+    """bf16 weights without weight decay whose rows TMA does not take (odd
+    widths; at 128 < T <= 256 every width): each row's 16-byte aligned interior
+    gets D = bf16(-lr s O) by one bulk reduce-add and the elements outside it by
+    single atomic adds. From W0 = 0 the step stores D; from any W0 (same G and
+    M) it must store bf16_rne(W0 + D), element for element. H is a multiple of
+    T, so no tile runs transposed; some right-edge tiles (9, 3, 11 and 3
+    columns) are narrower than one 16-byte chunk plus a phase, so some rows
+    have no interior at all."""
     G = synth.lowrank_noise(H, W, seed=T + W).cuda()
     M0 = synth.gaussian(H, W, 5, std=1e-3).cuda()
     W0 = synth.gaussian(H, W, 6, std=0.02, dtype=torch.bfloat16).cuda()

@@ -190,6 +190,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
   const int T = ns.T;
   const int64_t ncl = gridDim.x >> 1;
+  // bf16 weights without decay get their update without a read of W into the
+  // SM: the last epilogue writes D = bf16(-lr s O) into one shared-memory line
+  // per row (with the row's 16-byte phase), one thread per row adds the row's
+  // 16-byte aligned interior by a bulk reduce-add (at L2), the ends go by atomic
+  // adds. The lines lie in buffers the peer never writes: B0..B2 in CTA 0, B3
+  // and sC in CTA 1.
+  constexpr uint32_t PLROW = 2 * PT + 16;
+  const uint32_t lbase = sbase + (c == 0 ? 0u : sm_b(3));
+  bool rows_pending = false;     // this thread's bulk reduce-add still reads its line
+  bool rows_wait = false;        // the last tile used the lines: wait before rewriting them
 #pragma unroll 1
   for (int64_t tile = tile_begin + (blockIdx.x >> 1); tile < tile_end; tile += ncl) {
     const int mi = find_matrix(descs, ndesc, tile);
@@ -204,6 +214,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // output (or W) rows that allow 16-byte accesses: written by each thread
     // from its own row segment; otherwise staged and written coalesced by warps
     const bool vec_out = (d.flags & F_OUT_VEC) && (j0 * (out32 ? 4 : 2)) % 16 == 0;
+    const bool wbulk = STEP && !tr && !out32 && st.wd_factor == 1.f;
+    if (rows_wait) {                       // (the same for every thread of the CTA)
+      if (rows_pending) ptx::bulk_wait_read0();
+      rows_pending = false;
+      rows_wait = false;
+      named_sync(BAR_LINK, NTHREADS);
+    }
 
     // ---- prologue: U (momentum applied for a step, M written back) into
     // R_X = a U - e U_bf and the X_bf buffers; sums of squares
@@ -482,6 +499,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           float v[32];
           ptx::tmem_ld32_sync(t_x + xc, v);
           if (k == 0) scale32(v, sc_t);
+          if (wbulk) {                               // D into the row's line, or atomic adds
+            if (xr < xh) {
+              const uintptr_t g0 = reinterpret_cast<uintptr_t>(gptr(d.out, d.ld_out, i0 + xr, j0, false));
+              const uintptr_t ga = (g0 + 15) & ~uintptr_t(15);
+              const uintptr_t gb = (g0 + 2 * static_cast<uintptr_t>(xw)) & ~uintptr_t(15);
+              const uint32_t line = lbase + static_cast<uint32_t>(r) * PLROW + static_cast<uint32_t>(g0 & 15);
+              const float nls = -d.upd_scale;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int col = xc + j;
+                if (col < xw) {
+                  const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(nls * v[j]));
+                  const uintptr_t ge = g0 + 2 * static_cast<uintptr_t>(col);
+                  if (ge >= ga && ge < gb)
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(line + 2u * col), "h"(bits) : "memory");
+                  else
+                    ptx::red_add_bf16(reinterpret_cast<void*>(ge), bits);
+                }
+              }
+            }
+            continue;
+          }
           // last step. A transposed tile: out = X'^T (NS map), or W <- wd W -
           // lr s X'^T (step), the lanes writing consecutive columns of one row.
           if (!tr && vec_out) {                      // 16-byte stores of the own row segment
@@ -516,7 +555,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (last && !tr && !vec_out) {
+      if (last && wbulk) {
+        ptx::fence_proxy_async_smem();             // the lines, for the bulk reduce-add
+        named_sync(BAR_LINK, NTHREADS);
+        if (cq == 0 && xr < xh && !*abort_flag) {  // one thread per row
+          const uintptr_t g0 = reinterpret_cast<uintptr_t>(gptr(d.out, d.ld_out, i0 + xr, j0, false));
+          const uintptr_t ga = (g0 + 15) & ~uintptr_t(15);
+          const uintptr_t gb = (g0 + 2 * static_cast<uintptr_t>(xw)) & ~uintptr_t(15);
+          if (gb > ga) {
+            ptx::bulk_reduce_add_bf16(reinterpret_cast<void*>(ga),
+                                      lbase + static_cast<uint32_t>(r) * PLROW +
+                                          static_cast<uint32_t>(ga - (g0 & ~uintptr_t(15))),
+                                      static_cast<uint32_t>(gb - ga));
+            ptx::bulk_commit();
+            rows_pending = true;
+          }
+        }
+        rows_wait = true;
+      }
+      if (last && !tr && !vec_out && !wbulk) {
         // last step, the tile as it is: X' goes through sC (fp32) one
         // 128-column half at a time (the half held by column quarters 2 h2 and
         // 2 h2 + 1 was staged above for h2 = 0); warp w then writes rows
@@ -611,6 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  if (rows_pending) ptx::bulk_wait0();           // the reduce-adds have completed
   // ---- teardown: every product this CTA issued has completed, then both CTAs
   // leave together (the peer writes into this CTA's shared memory)
   if (issued && *abort_flag) {
