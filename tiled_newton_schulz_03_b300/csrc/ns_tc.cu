@@ -11,14 +11,16 @@
 //
 // CTA (one per SM, 20 warps = 5 per scheduler, so 96 registers per thread):
 //   warps 0-3   loader: brings the next stage's G (and M) into a staging buffer
-//               with TMA (plain loads for layouts TMA cannot describe), applies
-//               momentum (M <- mu M + G, stored back with TMA) and computes the
-//               per-tile sums of squares for the normalisation. Warp 0 also
-//               allocates and frees tensor memory.
+//               with TMA, and stores the previous stage's updated momentum back
+//               with TMA. Rows TMA cannot describe come in by bulk copies of
+//               their 16-byte aligned covers (or plain loads), and for those the
+//               loader applies momentum itself. Warp 0 also allocates and frees
+//               tensor memory.
 //   warps 4-11  slot 0, warps 12-19 slot 1 (8 warps each: lane quarter =
-//               warp % 4, column half = (warp - first) / 4). A slot's warps run
-//               the epilogue of each product and its first thread issues the
-//               slot's next product.
+//               warp % 4, column half = (warp - first) / 4). A slot's warps apply
+//               momentum to TMA-staged tiles, sum the squares for the
+//               normalisation, run the epilogue of each product, and one thread
+//               issues the slot's next product.
 // The two slots hold two independent stages; while the tensor core runs one
 // slot's product, the other slot's warps run their epilogue, so the serial
 // chain of a tile's 3K products never leaves the tensor pipe idle for long.
@@ -32,7 +34,8 @@
 //   sX  (smem 32 KB)   X in bf16, 128-byte swizzled, 128-byte rows: operand of
 //                      X X^T (K-major) and of C X (MN-major).
 //   sC  (smem 32 KB)   A in bf16 (operand of A A), then C in bf16 (operand of C X).
-//   R_A (TMEM, 128 columns)  accumulator of X X^T, then of A_bf A_bf.
+//   R_A (TMEM, 128 columns)  accumulator of X X^T, then of A_bf A_bf onto the
+//                      preload (b / c) A_bf + (e / c) I, so that C = c R_A.
 //   R_X (TMEM, 128 columns)  fp32 iterate: holds a X - e X_bf before C X_bf is
 //                      accumulated onto it, X' afterwards.
 // Rounding: with e = a - min(a, 1.5) and C = B + e I,
@@ -40,6 +43,10 @@
 // so X keeps fp32 precision in the a X term, and the bf16 operand C has its
 // spectrum (about [-2.8, 0] for the quintic's B) centred near zero, which keeps
 // its rounding small where a + B nearly cancels (rank-1 tiles).
+// Weight update (step): bf16 W without decay gets D = bf16(-lr s X') added at
+// L2, by a TMA reduce-add for 16-byte aligned rows or by row-wise bulk
+// reduce-adds of each row's aligned interior (plus atomic adds of the ends);
+// fp32 W and weight decay take a read-modify-write row pass.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

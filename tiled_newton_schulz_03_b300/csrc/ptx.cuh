@@ -125,9 +125,6 @@ __device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, float (&va)[32], u
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -283,27 +280,7 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared),
-// releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
 
-// try_wait with acquire at cluster scope (the arrivals come from the peer CTA)
-// and a suspend-time hint in nanoseconds.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity,
-                                                      uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
 
 // Generic-proxy writes to shared memory of any CTA of the cluster (this CTA's
 // included) made visible to the async proxy.
