@@ -181,6 +181,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     issue(p);                                  // CTA 0's issuer only
   };
 
+  // X_bf of this thread's columns of the other n-half (in the local X X^T
+  // operand) into the peer's C X operand, then its fence at cluster scope; run
+  // after a hand-off to X X^T, which does not read that block: the hand-offs
+  // before C X order these writes before it
+  auto peer_block = [&]() {
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      const int cl = (xc0 + 32 * ch) & 127;
+      uint32_t pkd[16];
+#pragma unroll
+      for (int qd = 0; qd < 4; ++qd) {
+        const uint4 u = ptx::ld_shared_v4(xb1 + bf_off(r, (cl >> 3) + qd));
+        pkd[4 * qd] = u.x; pkd[4 * qd + 1] = u.y; pkd[4 * qd + 2] = u.z; pkd[4 * qd + 3] = u.w;
+      }
+      st_bf16_32_remote(xb2_remote, r, cl, pkd);
+    }
+    ptx::fence_proxy_async_cluster();
+  };
+
   // The commit that completes acc_full comes from CTA 0's issuer, multicast by
   // the tensor core; what it orders is tensor memory, which the
   // tcgen05.fence::after_thread_sync below covers, so the wait needs CTA scope only.
@@ -246,9 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           for (int qd = 0; qd < 4; ++qd)
             ptx::st_shared_v4(xb2_local + bf_off(r, (cl >> 3) + qd), pkd[4 * qd], pkd[4 * qd + 1],
                               pkd[4 * qd + 2], pkd[4 * qd + 3]);
-        } else {
-          st_bf16_32_remote(xb2_remote, r, cl, pkd);
-        }
+        }                                            // the peer's block after the first hand-off
         const uint64_t a2 = pk2(cf0.a, cf0.a), ne2 = pk2(-cf0.e, -cf0.e);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -389,8 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
     }
     ptx::tmem_wait_st();
-    if (own) ptx::fence_proxy_async_smem();
-    else ptx::fence_proxy_async_cluster();   // this thread also wrote the peer's block
+    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     named_sync(BAR_LINK, NTHREADS);
     // tile norm: each CTA's sum (fixed order) goes to the peer; the cluster
@@ -408,6 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const float s2 = sc_t * sc_t;
     ptx::tc_fence_after();
     issue(0);                              // -> X X^T
+    if (!own) peer_block();                // only C X, two products later, reads it
 
 #pragma unroll 1
     for (int k = 0; k < K; ++k) {
@@ -629,24 +646,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
       if (!last) {
         hand_over(false, 0);                       // -> next X X^T (reads X_bf only)
-        if (!own) {
-          // X'_bf of this thread's columns of the other n-half (just written to
-          // the local X X^T operand) into the peer's C X operand, then its fence
-          // at cluster scope, while X X^T runs: only C X, two products later,
-          // reads that block, and the hand-offs before it order these writes
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            const int cl = (xc0 + 32 * ch) & 127;
-            uint32_t pkd[16];
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-              const uint4 u = ptx::ld_shared_v4(xb1 + bf_off(r, (cl >> 3) + qd));
-              pkd[4 * qd] = u.x; pkd[4 * qd + 1] = u.y; pkd[4 * qd + 2] = u.z; pkd[4 * qd + 3] = u.w;
-            }
-            st_bf16_32_remote(xb2_remote, r, cl, pkd);
-          }
-          ptx::fence_proxy_async_cluster();
-        }
+        if (!own) peer_block();                    // while X X^T runs
         // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
         // step's coefficients) for that step's C X, the first product to read
         // R_X; the hand-off before it waits for these stores.
