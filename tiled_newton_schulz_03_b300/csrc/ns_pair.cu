@@ -17,9 +17,9 @@
 //   X X^T  A: own rows of X, K = all 256 columns; B: the same rows (N split by CTA)
 //   A A^T  A and B: own rows of A_bf (A is symmetric)
 //   C X    A: own rows of C_bf; B: X restricted to the own n-half, K = all 256 rows,
-//          so each CTA needs the PEER's rows of its n-half: at the end of every
-//          step each CTA writes that block of its new X_bf into the peer's shared
-//          memory (distributed shared memory; no TMA multicast).
+//          so each CTA needs the PEER's rows of its n-half: once per step each CTA
+//          copies that block of its X_bf (one 32 KB bulk copy, shared memory to
+//          the peer's shared memory) while X X^T runs.
 // The two products' B operands sit at the same shared-memory offsets in both
 // CTAs, so X_bf is kept in four 128 x 128 buffers per CTA:
 //   B[c] = own rows x own half (X X^T, K-half c)  B[1-c] = own rows x other half
@@ -70,20 +70,24 @@ constexpr uint32_t SMEM_DYN = SM_END + 1024;
 struct PairCtl {
   uint64_t acc_full;     // the pair's last product is complete (multicast commit)
   uint64_t drain;        // abort path: every issued product has completed
+  uint64_t peer_in;      // the peer's block of the C X operand has arrived (bulk copy)
   uint32_t tmem_base;
   int abort_flag;
   float part[16];        // per warp: sum of squares of its elements
   float part_peer;       // the peer CTA's sum (written by the peer)
 };
 
-// 32 bf16 values -> 4 x 16-byte chunks of row r, columns [c, c + 32), of a
-// swizzled bf16 buffer in the PEER's shared memory (cluster address of its base)
-__device__ __forceinline__ void st_bf16_32_remote(uint32_t rbase, int r, int c,
-                                                  const uint32_t (&pkd)[16]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    ptx::st_cluster_v4(rbase + bf_off(r, (c >> 3) + q), pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2],
-                       pkd[4 * q + 3]);
+// Contiguous copy of `bytes` from this CTA's shared memory into the shared
+// memory of another CTA of the cluster (dst and bar: cluster addresses in that
+// CTA; both addresses 16-byte aligned, bytes a multiple of 16); the bytes
+// complete on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 template <bool STEP>
@@ -102,10 +106,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = &ctl.abort_flag;
   const uint32_t b_acc = ptx::smem_u32(&ctl.acc_full);
   const uint32_t b_drain = ptx::smem_u32(&ctl.drain);
+  const uint32_t b_peer = ptx::smem_u32(&ctl.peer_in);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(b_acc, 1);
     ptx::mbar_init(b_drain, 1);
+    ptx::mbar_init(b_peer, 1);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
   }
@@ -131,12 +137,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const uint32_t t_x = tbase + lane_off + 256u;   // R_X, columns 256..511
   const uint32_t sc = sbase + SM_C;
   // this thread's X_bf buffers: own half -> B[c] and B[2+c] (local); other half
-  // -> B[1-c] (local) and B[2+c] of the peer
+  // -> B[1-c] (local), which is copied as a whole into B[2+c] of the peer (the
+  // two buffers have the same layout)
   const uint32_t xb1 = sbase + sm_b(own ? static_cast<int>(c) : 1 - static_cast<int>(c));
   const uint32_t xb2_local = sbase + sm_b(2 + static_cast<int>(c));
-  const uint32_t xb2_remote = ptx::mapa_shared(sbase + sm_b(2 + static_cast<int>(c)), peer);
+  const uint32_t blk_src = sbase + sm_b(1 - static_cast<int>(c));
+  const uint32_t blk_dst = ptx::mapa_shared(xb2_local, peer);
+  const uint32_t b_peer_remote = ptx::mapa_shared(b_peer, peer);
 
   uint32_t acc_ph = 0;
+  uint32_t peer_ph = 0;          // phase of peer_in (waited by thread 0 before C X)
   bool issued = false;
 
   // product p of the tile (0: X X^T -> R_A; 1: A A^T -> R_A; 2: C X onto R_X)
@@ -164,40 +174,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     issued = true;
   };
 
-  // Hand-off after an epilogue: operands written (local and peer shared memory,
-  // tensor memory) -> product p. All threads of both CTAs meet at the cluster
-  // barrier (release / acquire at cluster scope), then CTA 0's issuer issues.
-  // Every thread of both CTAs makes the same sequence of hand-offs (same tiles,
-  // same steps), whatever the abort flag says.
+  // Hand-off after an epilogue: operands written (shared and tensor memory) ->
+  // product p. All threads of both CTAs meet at the cluster barrier (release /
+  // acquire at cluster scope), then CTA 0's issuer issues. Before C X, thread 0
+  // of each CTA first waits until the peer's block of this CTA's C X operand
+  // has arrived (copied two products earlier, so normally long done). Every
+  // thread of both CTAs makes the same sequence of hand-offs (same tiles, same
+  // steps), whatever the abort flag says.
   auto hand_over = [&](bool tmem_written, int p) {
     if (tmem_written) ptx::tmem_wait_st();
-    // Writes into the peer's shared memory (prologue, E3) are read only by the
-    // C X product (its B operand's peer block), two products later; their
-    // writers fence them at cluster scope right after writing them, off the
-    // chain, so every hand-off needs only this CTA's fence.
+    if (p == 2) {
+      if (threadIdx.x == 0) wait_bar(b_peer, peer_ph, wait_ns, abort_flag, err);
+      peer_ph ^= 1u;
+    }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     ptx::cluster_sync();
     issue(p);                                  // CTA 0's issuer only
   };
 
-  // X_bf of this thread's columns of the other n-half (in the local X X^T
-  // operand) into the peer's C X operand, then its fence at cluster scope; run
-  // after a hand-off to X X^T, which does not read that block: the hand-offs
-  // before C X order these writes before it
-  auto peer_block = [&]() {
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      const int cl = (xc0 + 32 * ch) & 127;
-      uint32_t pkd[16];
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        const uint4 u = ptx::ld_shared_v4(xb1 + bf_off(r, (cl >> 3) + qd));
-        pkd[4 * qd] = u.x; pkd[4 * qd + 1] = u.y; pkd[4 * qd + 2] = u.z; pkd[4 * qd + 3] = u.w;
-      }
-      st_bf16_32_remote(xb2_remote, r, cl, pkd);
-    }
-    ptx::fence_proxy_async_cluster();
+  // The peer block: thread 0 of each CTA arms peer_in for it (before a cluster
+  // barrier), and after that barrier thread 0 of the peer copies B[1-c] of the
+  // peer (its X_bf rows of this CTA's n-half, written before the barrier) into
+  // B[3-c] here. The copy runs while X X^T runs (which does not read B[3-c]);
+  // B[1-c] of the sender is rewritten only after the C X hand-off, by which time
+  // the copy has completed.
+  auto arm_peer_block = [&]() {
+    if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(b_peer, sm_b(1));
+  };
+  auto send_peer_block = [&]() {
+    if (threadIdx.x == 0) bulk_copy_to_cta(blk_dst, blk_src, sm_b(1), b_peer_remote);
   };
 
   // The commit that completes acc_full comes from CTA 0's issuer, multicast by
@@ -416,6 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < 16; ++i) part_self += ctl.part[i];
     if (threadIdx.x == 0)
       ptx::st_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&ctl.part_peer), peer), part_self);
+    arm_peer_block();
     ptx::cluster_sync();
     const float tot = (c == 0) ? part_self + ctl.part_peer : ctl.part_peer + part_self;
     float sc_t = 1.f;
@@ -424,7 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const float s2 = sc_t * sc_t;
     ptx::tc_fence_after();
     issue(0);                              // -> X X^T
-    if (!own) peer_block();                // only C X, two products later, reads it
+    send_peer_block();                     // only C X, two products later, reads it
 
 #pragma unroll 1
     for (int k = 0; k < K; ++k) {
@@ -645,8 +652,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         named_sync(BAR_LINK, NTHREADS);              // sC is free for the next tile
       }
       if (!last) {
+        arm_peer_block();
         hand_over(false, 0);                       // -> next X X^T (reads X_bf only)
-        if (!own) peer_block();                    // while X X^T runs
+        send_peer_block();                         // while X X^T runs
         // Off the chain, while X X^T runs: R_X = a X' - e X'_bf (the next
         // step's coefficients) for that step's C X, the first product to read
         // R_X; the hand-off before it waits for these stores.
@@ -679,6 +687,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     while (!ptx::mbar_try_wait(b_drain, 0) && ptx::globaltimer() - t0 < wait_ns) {
     }
   }
+  // a wait for the peer block may have given up on abort: its copy lands
+  // before either CTA leaves (a fresh barrier passes at once)
+  if (*abort_flag && threadIdx.x == 0) (void)ptx::mbar_wait_bounded(b_peer, peer_ph ^ 1u, wait_ns);
   ptx::tc_fence_before();
   ptx::cluster_sync();
   if (warp == 0) {
