@@ -478,6 +478,17 @@ def test_pair_kernel_small_K_and_fp32_input(K):
     assert torch.equal(o16, out.to(torch.bfloat16))      # one rounding of the same fp32 result
 
 
+@pytest.mark.parametrize("K,coeffs", [(5, SCHED), (3, (1.5, -0.5, 0.0)), (1, hm.QUINTIC)])
+def test_pair_kernel_many_tiles_per_cluster(K, coeffs):
+    """120 tiles of 256 x 256 on at most 74 clusters, so clusters run several
+    tiles back to back. Each step's arrival of the peer block (armed, copied,
+    waited on before C X, also on steps without A A) repeats across tiles."""
+    G = synth.lowrank_noise(3072, 2560, seed=9 + K)
+    out = hm.tiled_ns(G.cuda(), 256, K, coeffs=coeffs, path="tensor", out_dtype=torch.float32)
+    want = oracle.tiled_ns(f64(G), 256, K, coeffs)
+    assert rel_fro(f64(out), want) <= TOL_BF16
+
+
 @pytest.mark.parametrize("T", [256, 200])
 def test_pair_kernel_step_matches_oracle(T):
     shapes = [(768, 768), (300, 530), (1000, 300), (520, 1030)]
