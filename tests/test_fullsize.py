@@ -10,9 +10,9 @@ the 4096 x 4096 full-matrix map) it is compared in full.
 Tolerances as in test_parity.py: relative Frobenius error <= 2e-2 against the
 oracle for the bf16 tensor path, on the NS output and on the update W_new - W0;
 momentum (one fp32 FMA) to 1e-6. The bf16 weights start at zero, so the stored
-W_new = bf16(-lr s O) carries only bf16's own relative rounding (2^-9 per
-element) and the update is checked at 2e-2 with no allowance for the rounding
-of a non-zero W.
+W_new = bf16(-lr s O) carries only bf16's own relative rounding (at most 2^-8
+per element, its unit roundoff), and the update is checked at 2e-2 with no
+allowance for the rounding of a non-zero W.
 """
 
 import math

@@ -269,9 +269,10 @@ def _step_case(shapes, seed, mdtype=torch.float32, wdtype=torch.bfloat16, w0="au
     """Weights, gradients and a non-zero momentum buffer for a step test.
 
     Weights in bf16 start at zero (w0 "auto"): then W_new = bf16(-lr s O) and
-    the update is measured to bf16's own relative rounding (2^-9 per element),
-    far inside 2e-2, instead of being buried under the rounding of |W| ~ 0.02
-    (about 5 % of an update of lr * 0.08). fp32 weights start at N(0, 0.02^2).
+    the update is measured to bf16's own relative rounding (at most 2^-8 per
+    element, its unit roundoff), far inside 2e-2, instead of being buried
+    under the rounding of |W| ~ 0.02 (about 5 % of an update of lr * 0.08).
+    fp32 weights start at N(0, 0.02^2).
     """
     zero = w0 == "zero" or (w0 == "auto" and wdtype == torch.bfloat16)
     Ws = [(torch.zeros(H, W, dtype=wdtype) if zero else
