@@ -461,25 +461,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const MatDesc& d = descs[tf.mi];
           return reinterpret_cast<uintptr_t>(gptr(d.in, d.ld_in, tf.i0 + row % T, tf.j0, false));
         };
-        if (STEP) {
-#pragma unroll 1
+        // every stage row a warp copies or converts below (rows 32 wl .. 32 wl + 31
+        // here, and each round's share of rows further down) lies in one tile of
+        // the stage: warps 0-1 take the first of two stacked 64-row tiles
+        static_assert(TPS == 1 || TPS == 2, "stacked tiles per stage");
+        const TileRef tw_ref = (TPS == 2 && wl >= 2) ? ref[TPS - 1] : ref[0];
+        const bool tw_ok = tw_ref.mi >= 0;
+        const MatDesc* tw_d = descs + (tw_ok ? tw_ref.mi : 0);
+        const int64_t ld_mom = tw_d->ld_mom, ld_in = tw_d->ld_in;
+        float* const mom0 = (STEP && tw_ok)
+                                ? static_cast<float*>(tw_d->mom) + static_cast<int64_t>(tw_ref.i0) * ld_mom + tw_ref.j0
+                                : nullptr;
+        const uintptr_t gin0 = reinterpret_cast<uintptr_t>(tw_d->in) +
+                               (tw_ok ? 2 * (static_cast<int64_t>(tw_ref.i0) * ld_in + tw_ref.j0) : 0);
+        if (STEP && tw_ok) {
+          const int rl0 = (32 * wl) % T;
+#pragma unroll 4
           for (int i = 0; i < 32; ++i) {
-            const int row = 32 * wl + i;
-            const TileRef& tf = ref[row / T];
-            const int rl = row % T;
-            if (tf.mi < 0) continue;
-            const MatDesc& d = descs[tf.mi];
+            const int row = 32 * wl + i, rl = rl0 + i;
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
               const int c = ln + 32 * j;
-              const bool ok = rl < tf.h && c < tf.w;
-              const float* src = static_cast<const float*>(d.mom) +
-                                  (ok ? static_cast<int64_t>(tf.i0 + rl) * d.ld_mom + tf.j0 + c : 0);
+              const bool ok = rl < tw_ref.h && c < tw_ref.w;
+              const float* src = mom0 + (ok ? static_cast<int64_t>(rl) * ld_mom + c : 0);
               ptx::cp_async_4(sbase + SM_S0 + f32_off(row, c >> 2) + (c & 3) * 4, src, ok ? 4u : 0u);
             }
           }
-          ptx::cp_async_commit();
         }
+        if (STEP) ptx::cp_async_commit();
 #pragma unroll 1
         for (int rd = 0; rd < ROUNDS; ++rd) {
           uint32_t bytes = 0;
@@ -501,27 +510,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           rows_phase ^= 1u;
           if (STEP && rd == 0) ptx::cp_async_wait_all();   // this thread's momentum copies
           named_sync(1, LOADER_THREADS);                    // everyone's have landed
-#pragma unroll 1
+#pragma unroll 4
           for (int i = 0; i < RROWS / 4; ++i) {
+            if (!tw_ok) break;                            // absent tile: zero-filled above
             const int row = RROWS * rd + (RROWS / 4) * wl + i;
-            const TileRef& tf = ref[row / T];
             const int rl = row % T;
-            if (tf.mi < 0) continue;                      // absent tile: zero-filled above
-            const bool row_ok = rl < tf.h;                // padding rows of the tile: zeros
-            const MatDesc& d = descs[tf.mi];
+            const bool row_ok = rl < tw_ref.h;            // padding rows of the tile: zeros
             const uint32_t rowb = sbase + SM_S1 + (row - RROWS * rd) * ROWB +
-                                  static_cast<uint32_t>(row_src(row, tf) & 15);
+                                  static_cast<uint32_t>((gin0 + 2 * static_cast<uint64_t>(rl) * ld_in) & 15);
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
               const int c = ln + 32 * j;
               float u = 0.f;
-              if (row_ok && c < tf.w) {
+              if (row_ok && c < tw_ref.w) {
                 uint16_t gb;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(gb) : "r"(rowb + 2 * c));
                 u = __uint_as_float(static_cast<uint32_t>(gb) << 16);
                 if (STEP) {
                   const float mn = fmaf(st.mu, f32_at(sbase + SM_S0, row, c), u);
-                  st_val(d.mom, static_cast<int64_t>(tf.i0 + rl) * d.ld_mom + tf.j0 + c, true, mn);
+                  mom0[static_cast<int64_t>(rl) * ld_mom + c] = mn;
                   u = st.nesterov ? fmaf(st.mu, mn, u) : mn;
                 }
               }
