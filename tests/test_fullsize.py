@@ -205,3 +205,33 @@ def test_ragged_shapes_tile_schedule(K):
     for i, sl, W_ref, M_ref, W_init in regions:
         assert rel_fro(f64(Ms[i][sl]), M_ref) <= 1e-5
         check_update(f64(Ws[i][sl]), W_init, W_ref)         # three steps' total update
+
+
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_unaligned_rows_bit_identical_to_aligned_full_size(T):
+    """The ragged set's 2048 x 50257 matrix, two fused steps, stored once with its
+    own leading dimension (rows not 16-byte aligned: loaded and converted row by
+    row) and once inside a 2048 x 50264 buffer (16-byte aligned rows: TMA-staged,
+    or 16-byte row loads at T = 256). Both do the same arithmetic in the same
+    order, so every element of W and M must agree bit for bit: a stage that
+    reached its slot before it was complete, or a row taken from the wrong
+    place, would not."""
+    dev = torch.device("cuda", 0)
+    H, W = 2048, 50257
+    G0 = synth.lowrank_noise(H, W, seed=61, rank=8, device=dev)
+    W0 = synth.gaussian(H, W, seed=62, std=0.02, dtype=torch.bfloat16, device=dev)
+    M0 = synth.gaussian(H, W, seed=63, std=1e-3, device=dev)
+    res = []
+    for ld in (W, 50264):
+        def place(x):
+            buf = torch.zeros(H, ld, dtype=x.dtype, device=dev)
+            v = buf[:, :W]
+            v.copy_(x)
+            return v
+        G, Wt, M = place(G0), place(W0), place(M0)
+        for _ in range(2):
+            hm.step([Wt], [G], [M], T, 5, lr=0.02, mu=0.95, nesterov=True)
+        torch.cuda.synchronize()
+        res.append((Wt.clone(), M.clone()))
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])

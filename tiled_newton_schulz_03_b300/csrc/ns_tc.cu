@@ -85,7 +85,6 @@ struct Ctl {
   uint64_t st_full[2];    // loader -> slots: staging holds stage g (barrier g % 2)
   uint64_t st_empty;      // slot -> loader: staging has been read
   uint64_t st_loaded;     // TMA -> loader: staging bytes have landed
-  uint64_t rows_loaded;   // bulk row copies (unaligned bf16 rows) -> loader
   uint64_t drain[2];      // slot issuer: all its MMAs complete (abort path)
   uint32_t tmem_base;
   int abort_flag;
@@ -215,7 +214,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t b_full[2] = {ptx::smem_u32(&ctl.st_full[0]), ptx::smem_u32(&ctl.st_full[1])};
   const uint32_t b_empty = ptx::smem_u32(&ctl.st_empty);
   const uint32_t b_loaded = ptx::smem_u32(&ctl.st_loaded);
-  const uint32_t b_rows = ptx::smem_u32(&ctl.rows_loaded);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -225,7 +223,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     ptx::mbar_init(b_empty, 1);
     ptx::mbar_init(b_loaded, 1);
-    ptx::mbar_init(b_rows, LOADER_THREADS);
     ptx::fence_mbar_init();
     ctl.abort_flag = 0;
     ctl.ticket = 0;
@@ -250,7 +247,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // =============================================================== loader
     const int r = threadIdx.x;              // stage row
     int last_mi = -1;
-    uint32_t ld_phase = 0, rows_phase = 0;
+    uint32_t ld_phase = 0;
     // TMA-staged momentum of the stage last handed to a slot: the slot writes
     // M <- mu M + G into the staging buffer; once it has released the buffer,
     // thread 0 stores it to HBM and waits until the store has read it.
@@ -443,27 +440,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (rows_bulk) {
-        // Every row of G (bf16, rows not 16-byte aligned) comes in by one bulk
-        // copy of its 16-byte aligned cover (at most 15 bytes more on either
-        // side, inside the same 16-byte chunks, so always mapped memory), all
-        // 128 stage rows (T = 64) or 64 per round (T = 128) into SM_S1 at a
-        // stride of 2 T + 16 bytes;
-        // fp32 momentum by cp.async into the staging tile, all rows at once.
-        // The warps then read each row with the lanes along the columns,
-        // apply momentum (M written back, coalesced) and store U.
+        // Every row of G (bf16, rows not 16-byte aligned) comes in as its 16-byte
+        // aligned cover (at most 15 bytes more on either side, inside the same
+        // 16-byte chunks, so always mapped memory), one 16-byte cp.async per
+        // lane: all 128 stage rows (T = 64) or 64 per round (T = 128) into SM_S1
+        // at a stride of 2 T + 16 bytes; fp32 momentum by 4-byte cp.async into
+        // the staging tile, all rows at once. The warps then read each row with
+        // the lanes along the columns, apply momentum (M written back,
+        // coalesced) and store U.
         constexpr int ROWB = 2 * T + 16;
         constexpr int NJ = T / 32;
         // rows per round: all 128 when their covers fit in SM_S1 (T = 64), else 64
         constexpr int RROWS = (128 * ROWB <= 32768) ? 128 : 64;
         constexpr int ROUNDS = 128 / RROWS;
         const int ln = r & 31, wl = r >> 5;
-        auto row_src = [&](int row, const TileRef& tf) -> uintptr_t {
-          const MatDesc& d = descs[tf.mi];
-          return reinterpret_cast<uintptr_t>(gptr(d.in, d.ld_in, tf.i0 + row % T, tf.j0, false));
-        };
-        // every stage row a warp copies or converts below (rows 32 wl .. 32 wl + 31
-        // here, and each round's share of rows further down) lies in one tile of
-        // the stage: warps 0-1 take the first of two stacked 64-row tiles
+        // every stage row a warp copies and converts below lies in one tile of
+        // the stage: at T = 64 warps 0-1 take the first of two stacked 64-row
+        // tiles (rows 0-63), warps 2-3 the second
         static_assert(TPS == 1 || TPS == 2, "stacked tiles per stage");
         const TileRef tw_ref = (TPS == 2 && wl >= 2) ? ref[TPS - 1] : ref[0];
         const bool tw_ok = tw_ref.mi >= 0;
@@ -474,42 +467,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 : nullptr;
         const uintptr_t gin0 = reinterpret_cast<uintptr_t>(tw_d->in) +
                                (tw_ok ? 2 * (static_cast<int64_t>(tw_ref.i0) * ld_in + tw_ref.j0) : 0);
+        // A warp copies and converts only its own rows (round rd: stage rows
+        // RROWS rd + (RROWS / 4) wl + i), so it waits for its own copies alone.
         if (STEP && tw_ok) {
-          const int rl0 = (32 * wl) % T;
-#pragma unroll 4
-          for (int i = 0; i < 32; ++i) {
-            const int row = 32 * wl + i, rl = rl0 + i;
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-              const int c = ln + 32 * j;
-              const bool ok = rl < tw_ref.h && c < tw_ref.w;
-              const float* src = mom0 + (ok ? static_cast<int64_t>(rl) * ld_mom + c : 0);
-              ptx::cp_async_4(sbase + SM_S0 + f32_off(row, c >> 2) + (c & 3) * 4, src, ok ? 4u : 0u);
+          for (int rd = 0; rd < ROUNDS; ++rd) {
+#pragma unroll 4
+            for (int i = 0; i < RROWS / 4; ++i) {
+              const int row = RROWS * rd + (RROWS / 4) * wl + i, rl = row % T;
+#pragma unroll
+              for (int j = 0; j < NJ; ++j) {
+                const int c = ln + 32 * j;
+                const bool ok = rl < tw_ref.h && c < tw_ref.w;
+                const float* src = mom0 + (ok ? static_cast<int64_t>(rl) * ld_mom + c : 0);
+                ptx::cp_async_4(sbase + SM_S0 + f32_off(row, c >> 2) + (c & 3) * 4, src, ok ? 4u : 0u);
+              }
             }
           }
         }
-        if (STEP) ptx::cp_async_commit();
 #pragma unroll 1
         for (int rd = 0; rd < ROUNDS; ++rd) {
-          uint32_t bytes = 0;
-          uintptr_t lo = 0;
-          if (r / RROWS == rd) {
-            const TileRef& tf = ref[r / T];
-            if (tf.mi >= 0 && r % T < tf.h) {
-              const uintptr_t a = row_src(r, tf);
-              lo = a & ~uintptr_t(15);
-              bytes = static_cast<uint32_t>(((a + 2 * tf.w + 15) & ~uintptr_t(15)) - lo);
+          // the covers of this warp's rows of the round, 16 bytes per lane
+          if (tw_ok && !*abort_flag) {
+#pragma unroll 4
+            for (int i = 0; i < RROWS / 4; ++i) {
+              const int row = RROWS * rd + (RROWS / 4) * wl + i, rl = row % T;
+              const uintptr_t a = gin0 + 2 * static_cast<uint64_t>(rl) * ld_in;
+              const uintptr_t lo = a & ~uintptr_t(15);
+              const int nck = static_cast<int>((((a + 2 * tw_ref.w + 15) & ~uintptr_t(15)) - lo) >> 4);
+              if (rl < tw_ref.h && ln < nck)
+                ptx::cp_async_16(sbase + SM_S1 + (row - RROWS * rd) * ROWB + 16 * ln,
+                                 reinterpret_cast<const void*>(lo + 16 * ln));
             }
           }
-          if (!*abort_flag) {
-            ptx::mbar_arrive_expect_tx(b_rows, bytes);
-            if (bytes) ptx::bulk_load(sbase + SM_S1 + (r - RROWS * rd) * ROWB,
-                                      reinterpret_cast<const void*>(lo), bytes, b_rows);
-          }
-          wait_bar(b_rows, rows_phase, wait_ns, abort_flag, err);
-          rows_phase ^= 1u;
-          if (STEP && rd == 0) ptx::cp_async_wait_all();   // this thread's momentum copies
-          named_sync(1, LOADER_THREADS);                    // everyone's have landed
+          ptx::cp_async_commit();
+          ptx::cp_async_wait_all();                      // this warp's covers (and momentum)
+          __syncwarp();
 #pragma unroll 4
           for (int i = 0; i < RROWS / 4; ++i) {
             if (!tw_ok) break;                            // absent tile: zero-filled above
@@ -535,7 +528,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               f32_put(sbase + SM_S0, row, c, u);
             }
           }
-          named_sync(1, LOADER_THREADS);                    // SM_S1 is refilled next round
+          __syncwarp();                                   // this warp's covers are refilled next round
         }
       }
       if (any_tma) {
