@@ -198,16 +198,6 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
-// Contiguous global -> shared copy of `bytes` (a multiple of 16; both addresses
-// 16-byte aligned), completing `bytes` transaction bytes on the mbarrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // Element-wise add of a shared-memory box into global memory through a tensor
 // map (the addition happens at L2; the map's data type sets the arithmetic).
