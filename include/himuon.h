@@ -253,8 +253,7 @@ himuon_status himuon_wait_selftest(himuon_handle* handle, void* stream);
  * Larger tile counts are processed in sub-batches that fit.
  *
  * Set-up: the first call on a device (that device current) looks up the
- * array's device address with cudaGetSymbolAddress and caches it; make that
- * first call before any stream capture on the device.
+ * array's device address with cudaGetSymbolAddress and caches it.
  * Concurrency: all calls share the one array, whose contents persist from
  * call to call (nothing in it needs clearing: each call writes every byte it
  * reads before reading it). Calls whose work overlaps on the GPU race on the
