@@ -12,10 +12,10 @@
 // CTA (one per SM, 20 warps = 5 per scheduler, so 96 registers per thread):
 //   warps 0-3   loader: brings the next stage's G (and M) into a staging buffer
 //               with TMA, and stores the previous stage's updated momentum back
-//               with TMA. Rows TMA cannot describe come in by bulk copies of
-//               their 16-byte aligned covers (or plain loads), and for those the
-//               loader applies momentum itself. Warp 0 also allocates and frees
-//               tensor memory.
+//               with TMA. Rows TMA cannot describe come in as 16-byte cp.async
+//               copies of their 16-byte aligned covers (or plain loads), and
+//               for those the loader applies momentum itself. Warp 0 also
+//               allocates and frees tensor memory.
 //   warps 4-11  slot 0, warps 12-19 slot 1 (8 warps each: lane quarter =
 //               warp % 4, column half = (warp - first) / 4). A slot's warps apply
 //               momentum to TMA-staged tiles, sum the squares for the
@@ -298,9 +298,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
 
-      // bf16 rows that TMA cannot describe are fetched by bulk row copies when
-      // the whole stage takes that path (no TMA tile in it; fp32 momentum)
-      bool rows_bulk = false;
+      // bf16 rows that TMA cannot describe are fetched as their 16-byte aligned
+      // covers when the whole stage takes that path (no TMA tile in it; fp32
+      // momentum)
+      bool rows_cover = false;
       {
         bool ok = true;
 #pragma unroll
@@ -308,9 +309,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (ref[u].mi < 0) continue;
           const int f = descs[ref[u].mi].flags;
           if ((f & F_TMA) || (f & F_IN_FP32) || (STEP && (f & F_M_BF16))) ok = false;
-          else rows_bulk = true;
+          else rows_cover = true;
         }
-        rows_bulk = rows_bulk && ok;
+        rows_cover = rows_cover && ok;
       }
 
       if (any_tma && r == 0 && !*abort_flag) {
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int i = 0; i < 32; ++i)
 #pragma unroll
             for (int j = 0; j < NJ; ++j) f32_put(sbase + SM_S0, r0 + i, ln + 32 * j, 0.f);
-        } else if (!(descs[me.mi].flags & F_TMA) && !rows_bulk) {
+        } else if (!(descs[me.mi].flags & F_TMA) && !rows_cover) {
           const MatDesc& d = descs[me.mi];
           const bool in32 = d.flags & F_IN_FP32, m32 = !(d.flags & F_M_BF16);
           auto m_index = [&](int rl, int c) {
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (rows_bulk) {
+      if (rows_cover) {
         // Every row of G (bf16, rows not 16-byte aligned) comes in as its 16-byte
         // aligned cover (at most 15 bytes more on either side, inside the same
         // 16-byte chunks, so always mapped memory), one 16-byte cp.async per
