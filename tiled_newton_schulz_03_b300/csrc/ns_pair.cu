@@ -90,6 +90,13 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst, uint32_t src, uin
       : "memory");
 }
 
+// 16 bytes global -> shared (both 16-byte aligned); only the first src_bytes
+// are read, the rest of the 16 is zero-filled.
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 template <bool STEP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ns_pair_kernel(const MatDesc* __restrict__ descs, int ndesc, int64_t tile_begin,
@@ -286,7 +293,99 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       // warps and staged through sC
       const bool vec_rows = (d.flags & F_IN_VEC) && (j0 * (in32 ? 4 : 2)) % 16 == 0 &&
                             (!STEP || ((d.flags & F_M_VEC) && (j0 * (m16 ? 2 : 4)) % 16 == 0));
-      if (!tr && vec_rows) {
+      if (STEP && !tr && vec_rows && !in32 && !m16) {
+        // bf16 G and fp32 M, 16-byte aligned rows: one 128-column half at a time
+        // all warps copy the CTA's rows of G and M with 16-byte cp.async, the
+        // lanes along a row (4 and 8 cache lines per warp instruction), into
+        // shared memory that nothing else uses before this tile's first hand-off:
+        // M into sC, G into B[3-c], where the peer's block lands only after that
+        // hand-off. Chunk k of stage row q sits at chunk k ^ (q % 8), so the
+        // per-row reads below are conflict-free. Each thread then applies
+        // momentum to its row's 64 columns and puts M back in place, and the
+        // warps write M back to global memory row by row, coalesced. Positions
+        // outside the tile are zero-filled by the copies and not written back.
+        const uint32_t stg_g = sbase + sm_b(3 - static_cast<int>(c));   // 128 rows x 256 B
+        const uint32_t stg_m = sc;                                       // 128 rows x 512 B
+        const int rb = 128 * static_cast<int>(c);                        // first row of this CTA
+        float* const mbase = static_cast<float*>(d.mom);
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int cb = 128 * h2;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {                  // G: 128 rows x 16 chunks
+            const int id = static_cast<int>(threadIdx.x) + NTHREADS * k;
+            const int q = id >> 4, ck = id & 15, col = cb + 8 * ck;
+            const int nb = (rb + q < xh) ? 2 * max(0, min(8, xw - col)) : 0;
+            cp_async_16z(stg_g + q * 256 + ((ck ^ (q & 7)) << 4),
+                         gptr(d.in, d.ld_in, i0 + (nb ? rb + q : 0), j0 + (nb ? col : 0), false), nb);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {                  // M: 128 rows x 32 chunks
+            const int id = static_cast<int>(threadIdx.x) + NTHREADS * k;
+            const int q = id >> 5, ck = id & 31, col = cb + 4 * ck;
+            const int nb = (rb + q < xh) ? 4 * max(0, min(4, xw - col)) : 0;
+            cp_async_16z(stg_m + q * 512 + ((ck ^ (q & 7)) << 4),
+                         gptr(d.mom, d.ld_mom, i0 + (nb ? rb + q : 0), j0 + (nb ? col : 0), true), nb);
+          }
+          ptx::cp_async_commit();
+          ptx::cp_async_wait_all();
+          named_sync(BAR_LINK, NTHREADS);                // every warp's copies have landed
+          if ((cq >> 1) == h2) {
+            const uint64_t mu2 = pk2(st.mu, st.mu);
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch) {
+              const int xc = xc0 + 32 * ch, cl = xc - cb;
+              float u[32], mv[32];
+#pragma unroll
+              for (int qd = 0; qd < 4; ++qd) {
+                const uint4 w = ptx::ld_shared_v4(stg_g + r * 256 + ((((cl >> 3) + qd) ^ (r & 7)) << 4));
+                u[8 * qd + 0] = ptx::bf16lo(w.x); u[8 * qd + 1] = ptx::bf16hi(w.x);
+                u[8 * qd + 2] = ptx::bf16lo(w.y); u[8 * qd + 3] = ptx::bf16hi(w.y);
+                u[8 * qd + 4] = ptx::bf16lo(w.z); u[8 * qd + 5] = ptx::bf16hi(w.z);
+                u[8 * qd + 6] = ptx::bf16lo(w.w); u[8 * qd + 7] = ptx::bf16hi(w.w);
+              }
+#pragma unroll
+              for (int qd = 0; qd < 8; ++qd) {
+                const uint4 w = ptx::ld_shared_v4(stg_m + r * 512 + ((((cl >> 2) + qd) ^ (r & 7)) << 4));
+                mv[4 * qd + 0] = __uint_as_float(w.x); mv[4 * qd + 1] = __uint_as_float(w.y);
+                mv[4 * qd + 2] = __uint_as_float(w.z); mv[4 * qd + 3] = __uint_as_float(w.w);
+              }
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const uint64_t mn = fma2(mu2, pk2(mv[j], mv[j + 1]), pk2(u[j], u[j + 1]));
+                upk2(mn, mv[j], mv[j + 1]);
+                if (st.nesterov) upk2(fma2(mu2, mn, pk2(u[j], u[j + 1])), u[j], u[j + 1]);
+                else upk2(mn, u[j], u[j + 1]);
+              }
+#pragma unroll
+              for (int qd = 0; qd < 8; ++qd)
+                ptx::st_shared_v4(stg_m + r * 512 + ((((cl >> 2) + qd) ^ (r & 7)) << 4),
+                                  __float_as_uint(mv[4 * qd]), __float_as_uint(mv[4 * qd + 1]),
+                                  __float_as_uint(mv[4 * qd + 2]), __float_as_uint(mv[4 * qd + 3]));
+              consume(xc, u);
+            }
+          }
+          named_sync(BAR_LINK, NTHREADS);                // the half's new M is in sC
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int id = static_cast<int>(threadIdx.x) + NTHREADS * k;
+            const int q = id >> 5, ck = id & 31, col = cb + 4 * ck;
+            const int nv = (rb + q < xh) ? max(0, min(4, xw - col)) : 0;
+            if (nv > 0) {
+              const uint4 w = ptx::ld_shared_v4(stg_m + q * 512 + ((ck ^ (q & 7)) << 4));
+              float* mp = mbase + static_cast<int64_t>(i0 + rb + q) * d.ld_mom + j0 + col;
+              if (nv == 4) {
+                *reinterpret_cast<uint4*>(mp) = w;
+              } else {
+                mp[0] = __uint_as_float(w.x);
+                if (nv > 1) mp[1] = __uint_as_float(w.y);
+                if (nv > 2) mp[2] = __uint_as_float(w.z);
+              }
+            }
+          }
+          named_sync(BAR_LINK, NTHREADS);                // staging is refilled next half
+        }
+      } else if (!tr && vec_rows) {
 #pragma unroll 1
         for (int ch = 0; ch < 2; ++ch) {
           const int xc = xc0 + 32 * ch;
