@@ -631,6 +631,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
               const uintptr_t gb = (g0 + 2 * static_cast<uintptr_t>(xw)) & ~uintptr_t(15);
               const uint32_t line = lbase + static_cast<uint32_t>(r) * PLROW + static_cast<uint32_t>(g0 & 15);
               const float nls = -d.upd_scale;
+              if ((g0 & 15) == 0 && xc + 32 <= xw) {   // a 16-byte aligned row: all 32 inside
+                uint32_t pkd[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pkd[j] = ptx::pack_bf16x2(nls * v[2 * j], nls * v[2 * j + 1]);
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd)
+                  ptx::st_shared_v4(line + 2u * xc + 16u * qd, pkd[4 * qd], pkd[4 * qd + 1], pkd[4 * qd + 2],
+                                    pkd[4 * qd + 3]);
+                continue;
+              }
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const int col = xc + j;
